@@ -1,0 +1,431 @@
+#!/usr/bin/env python3
+"""Benchmark of one decode step of the stack-wide paged-FP8 attention path.
+
+One step = gk_kv_append (RoPE(k), E4M3 quantise, packed-K / plain-V scatter for
+every layer) + gk_decode_attn_stack (GQA decode attention over every layer
+through the full or trimmed sliding-window block table), on synthetic inputs
+from gk_inputs with the KV cache resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gk|reference]
+
+Prints ONE JSON line (rank 0).  `value` is layer*seq/s (layers x active rows
+per step / step time) over all ranks; `e2e` is the same metric with the step's
+inputs copied from pinned host memory and the output copied back inside the
+timed region; `roofline` is for the attention call (planner + persistent
+kernel): algorithmic bytes (KV bytes the step must read, counted exactly from
+the context lengths, plus q and out) / its CUDA-event duration, against the
+measured HBM copy bandwidth.  `--impl reference` times the oracle (plain C,
+one thread) on a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank runs an independent replica (no collective
+on the data path); the timing is barrier-bracketed and the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gk_inputs as gi  # noqa: E402
+
+METRIC = "decode-attn layer·seq/s and achieved HBM GB/s (% of roofline), 1 GB300"
+UNIT = "layer·seq/s"
+DEFAULT_WORKLOAD = "gptoss_b64"
+ATTN_SOURCES = ["paged_fp8_kv_gk_gb300/csrc/gk_kernels.cu", "paged_fp8_kv_gk_gb300/csrc/gk_device.cuh",
+                "paged_fp8_kv_gk_gb300/csrc/gk_internal.h"]
+
+
+# ------------------------------------------------------------------ distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, _, ws = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, rank=rank, world_size=ws)
+    return dist if ws > 1 else None
+
+
+def reduce_timing(local_ms: float, local_units: float, dist=None, device=None):
+    """(max elapsed ms over ranks, total units over ranks)."""
+    if dist is None:
+        return local_ms, local_units
+    import torch
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    u = torch.tensor([local_units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ------------------------------------------------------------------ helpers
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def attn_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ATTN_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per attention launch from a committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "attn_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_src_sha") != attn_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="gk_clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[3:7]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def workload_config(w, c, l2_note: str):
+    kind, _, arg = w.lengths.partition(":")
+    return {"workload": w.name, "num_layers": w.num_layers, "batch": w.batch,
+            "active_rows": int(c.active.sum()), "q_heads": w.num_q_heads,
+            "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+            "window": w.window, "context": f"{kind}:{arg}", "mean_context": float(c.lengths[c.active == 1].mean()),
+            "kv_layout": "per-group buffers [2,nb,kv,B,D], K packed [..,B/2,D,2], E4M3",
+            "l2": l2_note}
+
+
+# ------------------------------------------------------------------ CPU baseline (oracle)
+def oracle_sample(w, c, step_host, cache, budget_s: float, seed: int = 0, rows_max=None):
+    """Time the oracle (single-threaded C) on whole rows of the workload: for
+    each sampled row, every layer pair's append + attention for all kv heads.
+    Returns (layer*seq per second, layer*seqs done, seconds, rows)."""
+    import oracle.rows as orows
+    import torch
+    rng = np.random.default_rng(seed)
+    rows = rng.permutation(np.nonzero(c.active)[0])
+    done, spent, used = 0, 0.0, []
+    for b in rows:
+        b = int(b)
+        for j in range(w.num_layers // 2):
+            ids = np.concatenate([np.asarray(c.full_blocks[b], np.int64),
+                                  np.asarray(c.swa_blocks[b], np.int64)])
+            idx = torch.as_tensor(ids, device=cache[j].device)
+            kp = cache[j][0].index_select(0, idx).cpu().numpy().reshape(-1)
+            vp = cache[j][1].index_select(0, idx).cpu().numpy().reshape(-1)
+            t0 = time.perf_counter()
+            orows.row_pair_from_pool(w, c, step_host, kp, vp, j, b)
+            spent += time.perf_counter() - t0
+            done += 2
+        used.append(b)
+        if spent >= budget_s or (rows_max is not None and len(used) >= rows_max):
+            break
+    return done / spent, done, spent, used
+
+
+# ------------------------------------------------------------------ main arms
+def run_gk(args):
+    import torch
+    import paged_fp8_kv_gk_gb300 as gk
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dist = dist_init("nccl")
+    dev = torch.device("cuda", local_rank)
+    w = gi.get(args.workload)
+    c = gi.make_control(w)
+    st = gi.make_step(w, dev)
+    cache = gi.make_cache(w, c, dev)
+    shape = gk.Shape.make(**gi.shape_dict(w, c))
+    t = lambda a, dt: torch.as_tensor(np.ascontiguousarray(a)).to(dev, dt)  # noqa: E731
+    ctl = dict(cos=t(c.cos, torch.float32), sin=t(c.sin, torch.float32),
+               k_scale=t(c.k_scale, torch.float32), v_scale=t(c.v_scale, torch.float32),
+               bt_full=t(c.bt_full, torch.int32), bt_swa=t(c.bt_swa, torch.int32),
+               pos=t(c.pos, torch.int32), pos_w=t(c.pos_w, torch.int32),
+               upd_full=t(c.upd_full, torch.int32), upd_swa=t(c.upd_swa, torch.int32),
+               active=t(c.active, torch.uint8))
+    q, k_new, v_new = st["q"].contiguous(), st["k_new"].contiguous(), st["v_new"].contiguous()
+    kb, vb = gk.split_group_buffers(cache)
+    out = torch.empty(w.num_layers, w.batch, w.num_q_heads, w.head_dim, dtype=torch.bfloat16,
+                      device=dev)
+    ws = gk.new_workspace(shape, dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def append():
+        gk.gk_kv_append(shape, k_new, v_new, ctl["cos"], ctl["sin"], ctl["k_scale"],
+                        ctl["v_scale"], ctl["upd_full"], ctl["upd_swa"], ctl["active"], kb, vb,
+                        stream=sh)
+
+    def attention():
+        gk.gk_decode_attn_stack(shape, q, kb, vb, ctl["k_scale"], ctl["v_scale"], ctl["cos"],
+                                ctl["sin"], ctl["bt_full"], ctl["bt_swa"], ctl["pos"],
+                                ctl["pos_w"], ctl["active"], out, None, ws, stream=sh)
+
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        append()
+        attention()
+    torch.cuda.synchronize(dev)
+    if gk.gk_read_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    a0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    a1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clocks = ClockSampler(local_rank)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    ev0.record(stream)
+    for k in range(K):
+        append()
+        a0[k].record(stream)
+        attention()
+        a1[k].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    attn_ms = statistics.fmean(a0[k].elapsed_time(a1[k]) for k in range(K))
+    units = gi.layer_seqs(w, c)
+    max_ms, total_units = reduce_timing(elapsed_ms, units * K, dist, dev)
+    value = total_units / (max_ms / 1e3)
+    ms_per_step = max_ms / K
+
+    # ---- end to end: inputs from pinned host memory, output back to host
+    host_in = {k: v.cpu().pin_memory() for k, v in
+               dict(q=q, k_new=k_new, v_new=v_new, **ctl).items()}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for k_, v_ in host_in.items():
+            dev_in[k_].copy_(v_, non_blocking=True)
+        gk.gk_kv_append(shape, dev_in["k_new"], dev_in["v_new"], dev_in["cos"], dev_in["sin"],
+                        dev_in["k_scale"], dev_in["v_scale"], dev_in["upd_full"],
+                        dev_in["upd_swa"], dev_in["active"], kb, vb, stream=sh)
+        gk.gk_decode_attn_stack(shape, dev_in["q"], kb, vb, dev_in["k_scale"], dev_in["v_scale"],
+                                dev_in["cos"], dev_in["sin"], dev_in["bt_full"], dev_in["bt_swa"],
+                                dev_in["pos"], dev_in["pos_w"], dev_in["active"], out, None, ws,
+                                stream=sh)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(W):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms, e2e_units = reduce_timing(e0.elapsed_time(e1), units * K, dist, dev)
+    if gk.gk_read_device_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    # ---- roofline of the attention call
+    kv_bytes = gi.kv_bytes_read(w, c)
+    qo = gi.qo_bytes(w, c)
+    alg_bytes = kv_bytes + qo
+    peak, peak_kind = measured_peaks()
+    achieved = alg_bytes / (attn_ms / 1e3) / 1e9
+    traffic = recorded_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "precision": "KV E4M3 codes; q/out bf16; QK^T and PV on f16 tensor-core MMA with fp32 "
+                     "accumulation; fp32 online softmax",
+        "data": "synthetic (seeded gk_inputs workload)",
+        "config": workload_config(w, c, f"inputs larger than L2: {kv_bytes / 1e9:.2f} GB KV read per step"),
+        "impl": "gk",
+        "attn_ms": round(attn_ms, 4),
+        "append_ms": round(ms_per_step - attn_ms, 4),
+        "achieved_GBps": round(achieved, 1),
+        "kv_bytes_per_step": kv_bytes, "qo_bytes_per_step": qo,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "peak_source": peak_kind,
+                     "kernel": "gk_decode_attn_stack (plan_kernel + attn_kernel)",
+                     "alg_bytes_per_launch": alg_bytes},
+        "e2e": {"value": round(e2e_units / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "ms_per_step": round(e2e_ms / K, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * K,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = {k: gi.bf16_bits(v) for k, v in st.items()}
+        v_cpu, n_done, secs, used = oracle_sample(w, c, host, cache, args.cpu_budget)
+        line["cpu_baseline"] = {
+            "value": round(v_cpu, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{len(used)} rows x {w.num_layers} layers (all kv heads), oracle append + "
+                      f"fp64 attention, {secs:.1f} s of single-thread CPU"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle timed on the host cores: each step is one whole row of the
+    workload (every layer pair, every kv head)."""
+    import torch
+    rank, local_rank, world = dist_env()
+    if rank != 0:
+        return
+    w = gi.get(args.workload)
+    c = gi.make_control(w)
+    dev = torch.device("cuda", local_rank) if torch.cuda.is_available() else torch.device("cpu")
+    st = gi.make_step(w, dev)
+    cache = gi.make_cache(w, c, dev)
+    host = {k: gi.bf16_bits(v) for k, v in st.items()}
+    import oracle.rows as orows
+    rng = np.random.default_rng(7)
+    rows = rng.permutation(np.nonzero(c.active)[0])
+    pools = {}
+
+    def one_step(b):
+        spent = 0.0
+        for j in range(w.num_layers // 2):
+            kp, vp = pools[(b, j)]
+            t0 = time.perf_counter()
+            orows.row_pair_from_pool(w, c, host, kp, vp, j, b)
+            spent += time.perf_counter() - t0
+        return spent
+
+    need = args.warmup + args.steps
+    for s in range(need):
+        b = int(rows[s % len(rows)])
+        for j in range(w.num_layers // 2):
+            if (b, j) not in pools:
+                ids = np.concatenate([np.asarray(c.full_blocks[b], np.int64),
+                                      np.asarray(c.swa_blocks[b], np.int64)])
+                idx = torch.as_tensor(ids, device=cache[j].device)
+                pools[(b, j)] = (cache[j][0].index_select(0, idx).cpu().numpy().reshape(-1),
+                                 cache[j][1].index_select(0, idx).cpu().numpy().reshape(-1))
+    for s in range(args.warmup):
+        one_step(int(rows[s % len(rows)]))
+    total = 0.0
+    for s in range(args.steps):
+        total += one_step(int(rows[(args.warmup + s) % len(rows)]))
+    units = args.steps * w.num_layers
+    value = units / total
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded gk_inputs workload)",
+        "config": workload_config(w, c, "host memory"), "impl": "reference",
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step one row x {w.num_layers} layers (all kv heads): "
+                                   f"oracle append + fp64 attention, single thread"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["gk", "reference"], default="gk")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle CPU time for the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gk(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+/*
+ * gk.h -- C ABI of the GB300 (sm_103a) stack-wide paged-FP8 decode-attention library.
+ *
+ * One decode step of GPT-OSS-style attention over a whole layer stack, as the
+ * "GPT-OSS-120B giga-kernel decode" page describes it:
+ *   - section "Kernel contract": even layers are sliding-window (window 128),
+ *     odd layers are full attention; the block table, the KV write index and
+ *     the position are chosen by i % 2, and the KV buffer by i / 2; the
+ *     attention-control tensors (RoPE cos/sin, a full and a trimmed
+ *     sliding-window block table, an active mask, absolute and window-frame
+ *     positions, two KV-update indices) are shared by all layers;
+ *   - section "KV-cache layout (per-buffer, HMA-preserving)": one base-0 group
+ *     buffer [2, num_blocks, kv, block, d] per layer pair, K half then V half;
+ *     K is read through the packed FP8 view [.., block/2, d, 2], V is never
+ *     packed.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers unless a parameter says "host".
+ *   - The caller owns every buffer.  The library allocates nothing, keeps no
+ *     state between calls other than a per-device error word (see
+ *     gk_read_device_error) and cached device properties, and does not retain
+ *     pointers after a call returns.
+ *   - `stream` is a cudaStream_t passed as void*.  Calls are asynchronous and
+ *     stream-ordered: a call returns after validating its arguments and
+ *     enqueueing its kernels.  NULL means the legacy default stream.
+ *   - Errors: every entry point returns a gk_status and never aborts, traps or
+ *     prints.  Argument checks run on the host before anything is enqueued; a
+ *     failed check enqueues nothing.  Launch failures map to GK_ERR_CUDA.
+ *     Out-of-range data found on the device (a block id >= num_blocks, an
+ *     update slot outside the buffer, a position beyond its table row) makes
+ *     the kernel skip that access and set a bit in the device error word.
+ *
+ * Layouts (row-major, innermost last; Hkv = num_kv_heads, G = Hq / Hkv,
+ * B = block_size, D = head_dim, NL = num_layers, Bt = batch):
+ *   q, out            bf16  [NL, Bt, Hq, D]      q head h uses kv head h / G
+ *   k_new, v_new      bf16  [NL, Bt, Hkv, D]
+ *   cos, sin          fp32  [Bt, D/2]            rotate-half pairs (e, e + D/2)
+ *   k_scale, v_scale  fp32  [NL]                 code = E4M3(x / scale), value = code * scale
+ *   bt_full           int32 [Bt, max_blocks_full] physical block ids
+ *   bt_swa            int32 [Bt, max_blocks_swa]  trimmed rows: first entry = block of the window start
+ *   pos, pos_w        int32 [Bt]                  absolute / window-frame position of the new token
+ *   upd_full, upd_swa int32 [Bt]                  flat slot = block * B + offset
+ *   active            uint8 [Bt]                  0 = row skipped (no write, zero output)
+ *   k_bufs[j], v_bufs[j]  HOST arrays of NL/2 DEVICE pointers: the K and V halves of
+ *                     group buffer j, each num_blocks * Hkv * B * D bytes, 16-byte aligned.
+ *                     K byte (pb, h, t, e) = ((pb*Hkv + h)*(B/2) + t/2)*(2D) + 2e + (t & 1)
+ *                     V byte (pb, h, t, e) = ((pb*Hkv + h)*B + t)*D + e
+ * Supported shapes (version 1): D == 64, G == 8, B == 16 or a multiple of 32 up to 1024,
+ * NL even and <= 128, Bt <= 8192.  Other shapes return GK_ERR_UNSUPPORTED.
+ */
+#ifndef GK_H
+#define GK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GK_OK = 0,
+    GK_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, inconsistent shape */
+    GK_ERR_UNSUPPORTED = 2,   /* valid shape outside what this version implements */
+    GK_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small */
+    GK_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    GK_ERR_DEVICE_BOUNDS = 5  /* gk_read_device_error found a device-side error bit */
+} gk_status;
+
+/* Device error-word bits (gk_read_device_error). */
+#define GK_DEVERR_SLOT 0x1u     /* an update slot lies outside its group buffer: write skipped */
+#define GK_DEVERR_BLOCK 0x2u    /* a block-table entry is outside [0, num_blocks): read skipped */
+#define GK_DEVERR_POS 0x4u      /* a position is negative or beyond its table row */
+#define GK_DEVERR_TIMEOUT 0x8u  /* a shared-memory barrier wait hit its iteration limit */
+#define GK_DEVERR_PLAN 0x10u    /* the work plan did not fit the workspace */
+
+typedef struct {
+    int32_t num_layers;      /* NL, even: layer pairs (2j, 2j+1) share group buffer j */
+    int32_t batch;           /* Bt */
+    int32_t num_q_heads;     /* Hq */
+    int32_t num_kv_heads;    /* Hkv */
+    int32_t head_dim;        /* D */
+    int32_t block_size;      /* B, tokens per KV block */
+    int32_t num_blocks;      /* blocks per group buffer (one global scalar) */
+    int32_t window;          /* sliding window W of the even layers, in positions */
+    int32_t max_blocks_full; /* columns of bt_full */
+    int32_t max_blocks_swa;  /* columns of bt_swa; >= ceil((W + B - 1) / B) */
+} gk_shape;
+
+/*
+ * gk_kv_append -- write the new token's K and V into the group buffers.
+ * ("GPT-OSS-120B giga-kernel decode", sections "Kernel contract" (two
+ * KV-update indices) and "KV-cache layout" (packed K, plain V).)
+ *
+ * For every layer i, active row b and kv head h:
+ *   slot = (i even) ? upd_swa[b] : upd_full[b];  pb = slot / B;  t = slot % B
+ *   k' = RoPE(k_new[i,b,h,:], cos[b], sin[b]) in IEEE fp32, no fused multiply-add:
+ *        k'_e = k_e*c_e - k_{e+D/2}*s_e,  k'_{e+D/2} = k_{e+D/2}*c_e + k_e*s_e
+ *   K_{i/2}[packed (pb,h,t,e)] = E4M3(k'_e / k_scale[i])       (fp32 division, RNE)
+ *   V_{i/2}[plain  (pb,h,t,e)] = E4M3(v_new[i,b,h,e] / v_scale[i])
+ * E4M3 = round to nearest, ties to even mantissa, saturating to +-448; NaN -> 0x7F.
+ * Inactive rows write nothing.  No other byte of any buffer changes.
+ * Returns GK_ERR_INVALID_ARG for null pointers or inconsistent shapes.
+ */
+gk_status gk_kv_append(const gk_shape *shape, const void *k_new, const void *v_new,
+                       const float *cos, const float *sin, const float *k_scale,
+                       const float *v_scale, const int32_t *upd_full, const int32_t *upd_swa,
+                       const uint8_t *active, void *const *k_bufs, void *const *v_bufs,
+                       void *stream);
+
+/*
+ * gk_attn_workspace_bytes -- recommended workspace size for gk_decode_attn_stack.
+ * host_positions is reserved (may be NULL; not read).  Any workspace of at
+ * least gk_attn_workspace_min_bytes() works: the planner fits its split-KV
+ * partials into whatever capacity it is given (less capacity -> fewer, longer
+ * splits).  Returns 0 for an invalid or unsupported shape.
+ */
+size_t gk_attn_workspace_bytes(const gk_shape *shape, const int32_t *host_positions);
+size_t gk_attn_workspace_min_bytes(const gk_shape *shape);
+
+/*
+ * gk_decode_attn_stack -- GQA decode attention for all layers of one step.
+ * ("GPT-OSS-120B giga-kernel decode", section "Kernel contract"; the
+ * split-KV combine is the flash-decoding log-sum-exp merge.)
+ *
+ * For every layer i, row b, q head h (kv head kvh = h / G):
+ *   i odd  (full):   keys t in [0, pos[b]] through row b of bt_full
+ *   i even (window): keys t in [max(0, pos_w[b] - W + 1), pos_w[b]] through row b of bt_swa
+ *   q' = RoPE(q[i,b,h,:], cos[b], sin[b]);  k_t = decode(K_{i/2}) * k_scale[i];
+ *   v_t = decode(V_{i/2}) * v_scale[i];  s_t = q'.k_t / sqrt(D)
+ *   out[i,b,h,:] = bf16_rne( sum_t softmax(s)_t v_t );  out_f32 (optional) gets the fp32 value.
+ * Inactive rows get zeros.  The cache is read, never written: run gk_kv_append
+ * first on the same stream when the new token must be attended to.
+ * workspace: device memory, 256-byte aligned, ws_bytes >= gk_attn_workspace_min_bytes;
+ * it is overwritten by every call (do not share one workspace between calls
+ * that may overlap on the device).
+ * Returns GK_ERR_WORKSPACE for a missing/small/misaligned workspace,
+ * GK_ERR_INVALID_ARG for null or non-16-byte-aligned tensors.
+ */
+gk_status gk_decode_attn_stack(const gk_shape *shape, const void *q, void *const *k_bufs,
+                               void *const *v_bufs, const float *k_scale, const float *v_scale,
+                               const float *cos, const float *sin, const int32_t *bt_full,
+                               const int32_t *bt_swa, const int32_t *pos, const int32_t *pos_w,
+                               const uint8_t *active, void *out, float *out_f32,
+                               void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * gk_e4m3_quantize -- codes[i] = E4M3(x[i] / scale) with the same fp32
+ * division and encoder as gk_kv_append (for bulk KV ingest and checks).
+ * x, codes: device arrays of n elements.
+ */
+gk_status gk_e4m3_quantize(const float *x, float scale, uint8_t *codes, int64_t n, void *stream);
+
+/*
+ * gk_read_device_error -- synchronise `stream`, return the current device's
+ * error word (GK_DEVERR_* bits) in *bits, and clear it if `clear` != 0.
+ * Returns GK_ERR_DEVICE_BOUNDS when any bit was set, GK_OK otherwise.
+ */
+gk_status gk_read_device_error(void *stream, uint32_t *bits, int clear);
+
+/* Human-readable name of a status code (static string). */
+const char *gk_status_str(gk_status status);
+
+/* Library ABI version (1). */
+int32_t gk_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GK_H */

@@ -1,0 +1,214 @@
+"""Python binding of the GB300 stack-wide paged-FP8 decode-attention library.
+
+Argument marshalling only: every step of the decode path runs in the CUDA
+kernels of ``libgk.so`` (sources in ``csrc/``, ABI in ``include/gk.h``).  There
+is no CPU fallback: if the library cannot be built or loaded, or a tensor is not
+on a CUDA device, the calls raise.
+
+The functions carry the C names: ``gk_kv_append``, ``gk_decode_attn_stack``,
+``gk_attn_workspace_bytes``, ``gk_attn_workspace_min_bytes``,
+``gk_e4m3_quantize``, ``gk_read_device_error``, ``gk_status_str``,
+``gk_abi_version``.  Tensors are torch tensors; the stream defaults to torch's
+current stream on the tensors' device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from typing import Optional, Sequence
+
+from . import build as _build
+
+GK_OK, GK_ERR_INVALID_ARG, GK_ERR_UNSUPPORTED, GK_ERR_WORKSPACE, GK_ERR_CUDA, \
+    GK_ERR_DEVICE_BOUNDS = range(6)
+GK_DEVERR_SLOT, GK_DEVERR_BLOCK, GK_DEVERR_POS, GK_DEVERR_TIMEOUT, GK_DEVERR_PLAN = \
+    0x1, 0x2, 0x4, 0x8, 0x10
+
+HEADER = os.path.join(_build.INCLUDE, "gk.h")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GkError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {gk_status_str(status)} ({status})")
+
+
+class Shape(ctypes.Structure):
+    """gk_shape: all int32."""
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_layers", "batch", "num_q_heads", "num_kv_heads", "head_dim",
+        "block_size", "num_blocks", "window", "max_blocks_full", "max_blocks_swa")]
+
+    @classmethod
+    def make(cls, **kw) -> "Shape":
+        return cls(**{k: int(v) for k, v in kw.items()})
+
+
+def declared_functions() -> list:
+    """Names of the functions include/gk.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gk_[a-z0-9_]+)\s*\(", text)))
+
+
+def lib(build_if_needed: bool = True) -> ctypes.CDLL:
+    """Load libgk.so (building it with nvcc first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build_if_needed else _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: run paged_fp8_kv_gk_gb300.build.build()")
+            L = ctypes.CDLL(path)
+            vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+            sp = ctypes.POINTER(Shape)
+            L.gk_status_str.restype = ctypes.c_char_p
+            L.gk_status_str.argtypes = [ctypes.c_int]
+            L.gk_abi_version.restype = i32
+            L.gk_abi_version.argtypes = []
+            L.gk_kv_append.restype = ctypes.c_int
+            L.gk_kv_append.argtypes = [sp] + [vp] * 12
+            L.gk_attn_workspace_bytes.restype = sz
+            L.gk_attn_workspace_bytes.argtypes = [sp, vp]
+            L.gk_attn_workspace_min_bytes.restype = sz
+            L.gk_attn_workspace_min_bytes.argtypes = [sp]
+            L.gk_decode_attn_stack.restype = ctypes.c_int
+            L.gk_decode_attn_stack.argtypes = [sp] + [vp] * 15 + [sz, vp]
+            L.gk_e4m3_quantize.restype = ctypes.c_int
+            L.gk_e4m3_quantize.argtypes = [vp, ctypes.c_float, vp, i64, vp]
+            L.gk_read_device_error.restype = ctypes.c_int
+            L.gk_read_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+            _lib = L
+    return _lib
+
+
+# --------------------------------------------------------------- marshalling
+def _ptr(t, dtype=None, name="tensor", allow_none=False):
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _ptr_array(ts: Sequence, name: str):
+    arr = (ctypes.c_void_p * len(ts))(*[_ptr(t, None, f"{name}[{i}]") for i, t in enumerate(ts)])
+    return arr
+
+
+def _stream(stream, like=None):
+    if stream is None:
+        import torch
+        dev = like.device if like is not None and hasattr(like, "device") else None
+        return torch.cuda.current_stream(dev).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != GK_OK:
+        raise GkError(status, where)
+
+
+def _as_shape(shape) -> Shape:
+    if isinstance(shape, Shape):
+        return shape
+    return Shape.make(**shape)
+
+
+# --------------------------------------------------------------- entry points
+def gk_status_str(status: int) -> str:
+    return lib().gk_status_str(int(status)).decode()
+
+
+def gk_abi_version() -> int:
+    return int(lib().gk_abi_version())
+
+
+def gk_attn_workspace_bytes(shape) -> int:
+    return int(lib().gk_attn_workspace_bytes(ctypes.byref(_as_shape(shape)), None))
+
+
+def gk_attn_workspace_min_bytes(shape) -> int:
+    return int(lib().gk_attn_workspace_min_bytes(ctypes.byref(_as_shape(shape))))
+
+
+def gk_kv_append(shape, k_new, v_new, cos, sin, k_scale, v_scale, upd_full, upd_swa, active,
+                 k_bufs, v_bufs, stream=None) -> None:
+    import torch
+    sh = _as_shape(shape)
+    st = lib().gk_kv_append(
+        ctypes.byref(sh), _ptr(k_new, torch.bfloat16, "k_new"), _ptr(v_new, torch.bfloat16, "v_new"),
+        _ptr(cos, torch.float32, "cos"), _ptr(sin, torch.float32, "sin"),
+        _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
+        _ptr(upd_full, torch.int32, "upd_full"), _ptr(upd_swa, torch.int32, "upd_swa"),
+        _ptr(active, torch.uint8, "active"),
+        ctypes.cast(_ptr_array(k_bufs, "k_bufs"), ctypes.c_void_p),
+        ctypes.cast(_ptr_array(v_bufs, "v_bufs"), ctypes.c_void_p), _stream(stream, k_new))
+    _check(st, "gk_kv_append")
+
+
+def gk_decode_attn_stack(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, bt_full, bt_swa,
+                         pos, pos_w, active, out, out_f32=None, workspace=None,
+                         stream=None) -> None:
+    import torch
+    sh = _as_shape(shape)
+    if workspace is None:
+        raise ValueError("workspace is required (size: gk_attn_workspace_bytes(shape))")
+    st = lib().gk_decode_attn_stack(
+        ctypes.byref(sh), _ptr(q, torch.bfloat16, "q"),
+        ctypes.cast(_ptr_array(k_bufs, "k_bufs"), ctypes.c_void_p),
+        ctypes.cast(_ptr_array(v_bufs, "v_bufs"), ctypes.c_void_p),
+        _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
+        _ptr(cos, torch.float32, "cos"), _ptr(sin, torch.float32, "sin"),
+        _ptr(bt_full, torch.int32, "bt_full"), _ptr(bt_swa, torch.int32, "bt_swa"),
+        _ptr(pos, torch.int32, "pos"), _ptr(pos_w, torch.int32, "pos_w"),
+        _ptr(active, torch.uint8, "active"), _ptr(out, torch.bfloat16, "out"),
+        _ptr(out_f32, torch.float32, "out_f32", allow_none=True),
+        _ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()), _stream(stream, q))
+    _check(st, "gk_decode_attn_stack")
+
+
+def gk_e4m3_quantize(x, scale: float, codes, stream=None) -> None:
+    import torch
+    st = lib().gk_e4m3_quantize(_ptr(x, torch.float32, "x"), float(scale),
+                                _ptr(codes, torch.uint8, "codes"), int(x.numel()),
+                                _stream(stream, x))
+    _check(st, "gk_e4m3_quantize")
+
+
+def gk_read_device_error(stream=None, clear: bool = True) -> int:
+    """Synchronise the stream and return (and by default clear) the device
+    error word: GK_DEVERR_* bits, 0 when nothing went out of range."""
+    bits = ctypes.c_uint32(0)
+    st = lib().gk_read_device_error(_stream(stream), ctypes.byref(bits), 1 if clear else 0)
+    if st not in (GK_OK, GK_ERR_DEVICE_BOUNDS):
+        raise GkError(st, "gk_read_device_error")
+    return int(bits.value)
+
+
+def split_group_buffers(bufs: Sequence):
+    """Group buffers [2, nb, kv, B, D] -> (K halves, V halves) as the ABI takes them."""
+    return [b[0] for b in bufs], [b[1] for b in bufs]
+
+
+def new_workspace(shape, device="cuda"):
+    import torch
+    n = gk_attn_workspace_bytes(shape)
+    if n == 0:
+        raise GkError(GK_ERR_UNSUPPORTED, "gk_attn_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device)

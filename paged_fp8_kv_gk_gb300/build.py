@@ -1,0 +1,83 @@
+"""Build the CUDA library (libgk.so) in-tree with nvcc for sm_103a.
+
+Usage: ``python -m paged_fp8_kv_gk_gb300.build`` or ``build()`` from Python.
+Translation units compile in parallel and link into one shared library with
+the CUDA runtime linked statically, so loading it needs only the driver.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(HERE, "csrc")
+BUILD_DIR = os.path.join(HERE, "_build")
+LIB_NAME = "libgk.so"
+LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
+ROOT = os.path.dirname(HERE)
+INCLUDE = os.path.join(ROOT, "include")
+
+SOURCES = ["gk_kernels.cu", "gk_api.cu"]
+HEADERS = ["gk_device.cuh", "gk_internal.h"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
+              "--expt-relaxed-constexpr", "-Xptxas", "-v"]
+
+
+def _nvcc() -> str:
+    cand = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    p = os.path.join(cand, "bin", "nvcc")
+    if os.path.exists(p):
+        return p
+    w = shutil.which("nvcc")
+    if not w:
+        raise RuntimeError("nvcc not found (set CUDA_HOME)")
+    return w
+
+
+def _stale() -> bool:
+    if not os.path.exists(LIB_PATH):
+        return True
+    t = os.path.getmtime(LIB_PATH)
+    deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, "gk.h")]
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile every translation unit and link libgk.so; returns its path."""
+    if not force and not _stale():
+        return LIB_PATH
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    nvcc = _nvcc()
+    procs = []
+    objs = []
+    for src in SOURCES:
+        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        log = obj + ".log"
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
+        f = open(log, "w")
+        procs.append((subprocess.Popen(cmd, stdout=f, stderr=subprocess.STDOUT), f, log, cmd))
+        objs.append(obj)
+    failed = []
+    for p, f, log, cmd in procs:
+        rc = p.wait()
+        f.close()
+        if rc != 0 or verbose:
+            with open(log) as fh:
+                text = fh.read()
+            if rc != 0:
+                failed.append(" ".join(cmd) + "\n" + text)
+            elif verbose:
+                sys.stderr.write(text)
+    if failed:
+        raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
+    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.check_call([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"])
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose=True))

@@ -1,0 +1,253 @@
+// gk_api.cu -- extern "C" entry points declared in include/gk.h: argument
+// validation, workspace layout and kernel launches.  No allocation.
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include "gk_internal.h"
+
+namespace gk {
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by all entry points.  Returns GK_OK, GK_ERR_INVALID_ARG
+// (inconsistent) or GK_ERR_UNSUPPORTED (valid but outside version 1).
+static gk_status check_shape(const gk_shape* s) {
+  if (!s) return GK_ERR_INVALID_ARG;
+  if (s->num_layers < 2 || (s->num_layers & 1) || s->batch < 1 || s->num_q_heads < 1 ||
+      s->num_kv_heads < 1 || s->head_dim < 2 || s->block_size < 2 || (s->block_size & 1) ||
+      s->num_blocks < 1 || s->window < 1 || s->max_blocks_full < 1 || s->max_blocks_swa < 1 ||
+      s->num_q_heads % s->num_kv_heads != 0)
+    return GK_ERR_INVALID_ARG;
+  if (s->num_layers > 2 * kMaxGroups || s->batch > kMaxBatch || s->head_dim != kHeadDim ||
+      s->num_q_heads / s->num_kv_heads != kGroup ||
+      !(s->block_size == 16 || (s->block_size % kStageTok == 0 && s->block_size <= 1024)))
+    return GK_ERR_UNSUPPORTED;
+  // the trimmed window row must hold every block a window can touch
+  const int64_t need_swa = (int64_t(s->window) + s->block_size - 1 + s->block_size - 1) / s->block_size;
+  if (s->max_blocks_swa < need_swa) return GK_ERR_INVALID_ARG;
+  // flat slots (block * B + offset) are int32
+  if (int64_t(s->num_blocks) * s->block_size > INT32_MAX) return GK_ERR_UNSUPPORTED;
+  if (int64_t(s->max_blocks_full) * s->block_size > INT32_MAX / 2) return GK_ERR_UNSUPPORTED;
+  return GK_OK;
+}
+
+static int64_t recommended_cap(const gk_shape& s) {
+  const int64_t max_tok = int64_t(s.max_blocks_full) * s.block_size;
+  if (max_tok <= kMinSplit) return 0;
+  const int64_t per_row = (max_tok + kMinSplit - 1) / kMinSplit;
+  const int64_t a = int64_t(s.batch) * (per_row < kMaxSplitsPerRow ? per_row : kMaxSplitsPerRow);
+  const int64_t b = 2 * int64_t(s.batch) + 256;
+  return a < b ? a : b;
+}
+
+WsLayout ws_layout(const gk_shape& s, size_t ws_bytes) {
+  WsLayout L;
+  const int64_t planes = int64_t(s.num_layers / 2) * s.num_kv_heads;
+  const size_t rec = size_t(kPartialFloats) * sizeof(float);
+  // fixed part, with the entry list sized for `cap` extra entries below
+  size_t off = 0;
+  L.hdr = off;
+  off = align256(off + kHdrWords * sizeof(int32_t));
+  const size_t after_hdr = off;
+  auto place = [&](int64_t cap) {
+    size_t o = after_hdr;
+    L.entries = o;
+    o = align256(o + size_t(s.batch + cap) * sizeof(int32_t));
+    L.swa_list = o;
+    o = align256(o + size_t(s.batch) * sizeof(int32_t));
+    L.zero_list = o;
+    o = align256(o + size_t(s.batch) * sizeof(int32_t));
+    L.ns = o;
+    o = align256(o + size_t(s.batch) * sizeof(int32_t));
+    L.part_base = o;
+    o = align256(o + size_t(s.batch) * sizeof(int32_t));
+    L.tickets = o;
+    o = align256(o + size_t(planes) * s.batch * sizeof(int32_t));
+    L.partials = o;
+    o = align256(o + size_t(cap) * size_t(planes) * rec);
+    L.total = o;
+    L.cap = cap;
+    L.max_entries = s.batch + cap;
+  };
+  if (ws_bytes == 0) {
+    place(recommended_cap(s));
+    return L;
+  }
+  place(0);
+  const size_t fixed = L.total;
+  int64_t cap = 0;
+  if (ws_bytes > fixed + 512) {
+    cap = int64_t((ws_bytes - fixed - 512) / (size_t(planes) * rec + sizeof(int32_t)));
+    const int64_t cmax = int64_t(s.batch) * kMaxSplitsPerRow;
+    if (cap > cmax) cap = cmax;
+  }
+  place(cap);
+  while (cap > 0 && L.total > ws_bytes) place(--cap);
+  return L;
+}
+
+}  // namespace gk
+
+using namespace gk;
+
+extern "C" {
+
+const char* gk_status_str(gk_status st) {
+  switch (st) {
+    case GK_OK: return "GK_OK";
+    case GK_ERR_INVALID_ARG: return "GK_ERR_INVALID_ARG";
+    case GK_ERR_UNSUPPORTED: return "GK_ERR_UNSUPPORTED";
+    case GK_ERR_WORKSPACE: return "GK_ERR_WORKSPACE";
+    case GK_ERR_CUDA: return "GK_ERR_CUDA";
+    case GK_ERR_DEVICE_BOUNDS: return "GK_ERR_DEVICE_BOUNDS";
+  }
+  return "GK_ERR_UNKNOWN";
+}
+
+int32_t gk_abi_version(void) { return 1; }
+
+gk_status gk_kv_append(const gk_shape* shape, const void* k_new, const void* v_new,
+                       const float* cos, const float* sin, const float* k_scale,
+                       const float* v_scale, const int32_t* upd_full, const int32_t* upd_swa,
+                       const uint8_t* active, void* const* k_bufs, void* const* v_bufs,
+                       void* stream) {
+  const gk_status st = check_shape(shape);
+  if (st != GK_OK) return st;
+  if (!k_new || !v_new || !cos || !sin || !k_scale || !v_scale || !upd_full || !upd_swa ||
+      !active || !k_bufs || !v_bufs)
+    return GK_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new)) return GK_ERR_INVALID_ARG;
+  AppendParams p;
+  memset(&p, 0, sizeof(p));
+  const int groups = shape->num_layers / 2;
+  for (int j = 0; j < groups; ++j) {
+    if (!k_bufs[j] || !v_bufs[j] || !aligned16(k_bufs[j]) || !aligned16(v_bufs[j]))
+      return GK_ERR_INVALID_ARG;
+    p.kb[j] = static_cast<uint8_t*>(k_bufs[j]);
+    p.vb[j] = static_cast<uint8_t*>(v_bufs[j]);
+  }
+  p.k_new = static_cast<const uint16_t*>(k_new);
+  p.v_new = static_cast<const uint16_t*>(v_new);
+  p.cosb = cos;
+  p.sinb = sin;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.upd_full = upd_full;
+  p.upd_swa = upd_swa;
+  p.active = active;
+  p.NL = shape->num_layers;
+  p.Bt = shape->batch;
+  p.Hkv = shape->num_kv_heads;
+  p.B = shape->block_size;
+  p.nb = shape->num_blocks;
+  return launch_append(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GK_OK : GK_ERR_CUDA;
+}
+
+size_t gk_attn_workspace_bytes(const gk_shape* shape, const int32_t* host_positions) {
+  (void)host_positions;
+  if (check_shape(shape) != GK_OK) return 0;
+  return ws_layout(*shape, 0).total;
+}
+
+size_t gk_attn_workspace_min_bytes(const gk_shape* shape) {
+  if (check_shape(shape) != GK_OK) return 0;
+  WsLayout L = ws_layout(*shape, 1);  // smallest layout: no partial capacity
+  return L.total;
+}
+
+gk_status gk_decode_attn_stack(const gk_shape* shape, const void* q, void* const* k_bufs,
+                               void* const* v_bufs, const float* k_scale, const float* v_scale,
+                               const float* cos, const float* sin, const int32_t* bt_full,
+                               const int32_t* bt_swa, const int32_t* pos, const int32_t* pos_w,
+                               const uint8_t* active, void* out, float* out_f32, void* workspace,
+                               size_t ws_bytes, void* stream) {
+  const gk_status st = check_shape(shape);
+  if (st != GK_OK) return st;
+  if (!q || !k_bufs || !v_bufs || !k_scale || !v_scale || !cos || !sin || !bt_full || !bt_swa ||
+      !pos || !pos_w || !active || !out)
+    return GK_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || (out_f32 && !aligned16(out_f32)) || !aligned16(cos) ||
+      !aligned16(sin))
+    return GK_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return GK_ERR_WORKSPACE;
+  const WsLayout L = ws_layout(*shape, ws_bytes);
+  if (L.total > ws_bytes) return GK_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  const int groups = shape->num_layers / 2;
+  for (int j = 0; j < groups; ++j) {
+    if (!k_bufs[j] || !v_bufs[j] || !aligned16(k_bufs[j]) || !aligned16(v_bufs[j]))
+      return GK_ERR_INVALID_ARG;
+    p.kb[j] = static_cast<const uint8_t*>(k_bufs[j]);
+    p.vb[j] = static_cast<const uint8_t*>(v_bufs[j]);
+  }
+  p.q = static_cast<const uint16_t*>(q);
+  p.out = static_cast<uint16_t*>(out);
+  p.out_f32 = out_f32;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.cosb = cos;
+  p.sinb = sin;
+  p.bt_full = bt_full;
+  p.bt_swa = bt_swa;
+  p.pos = pos;
+  p.pos_w = pos_w;
+  p.hdr = reinterpret_cast<const int32_t*>(ws + L.hdr);
+  p.queue = reinterpret_cast<int32_t*>(ws + L.hdr) + kHdrQueue;
+  p.entries = reinterpret_cast<const int32_t*>(ws + L.entries);
+  p.swa_list = reinterpret_cast<const int32_t*>(ws + L.swa_list);
+  p.zero_list = reinterpret_cast<const int32_t*>(ws + L.zero_list);
+  p.ns = reinterpret_cast<const int32_t*>(ws + L.ns);
+  p.part_base = reinterpret_cast<const int32_t*>(ws + L.part_base);
+  p.tickets = reinterpret_cast<int32_t*>(ws + L.tickets);
+  p.partials = reinterpret_cast<float*>(ws + L.partials);
+  p.cap = L.cap;
+  p.NL = shape->num_layers;
+  p.Bt = shape->batch;
+  p.Hq = shape->num_q_heads;
+  p.Hkv = shape->num_kv_heads;
+  p.B = shape->block_size;
+  p.nb = shape->num_blocks;
+  p.W = shape->window;
+  p.MBF = shape->max_blocks_full;
+  p.MBS = shape->max_blocks_swa;
+
+  PlanParams pl;
+  memset(&pl, 0, sizeof(pl));
+  pl.pos = pos;
+  pl.active = active;
+  pl.hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
+  pl.entries = reinterpret_cast<int32_t*>(ws + L.entries);
+  pl.swa_list = reinterpret_cast<int32_t*>(ws + L.swa_list);
+  pl.zero_list = reinterpret_cast<int32_t*>(ws + L.zero_list);
+  pl.ns = reinterpret_cast<int32_t*>(ws + L.ns);
+  pl.part_base = reinterpret_cast<int32_t*>(ws + L.part_base);
+  pl.tickets = reinterpret_cast<int32_t*>(ws + L.tickets);
+  pl.cap = L.cap;
+  pl.NL = shape->num_layers;
+  pl.Bt = shape->batch;
+  pl.Hkv = shape->num_kv_heads;
+  return launch_attention(pl, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GK_OK
+                                                                                   : GK_ERR_CUDA;
+}
+
+gk_status gk_e4m3_quantize(const float* x, float scale, uint8_t* codes, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (!x || !codes))) return GK_ERR_INVALID_ARG;
+  return launch_quantize(x, scale, codes, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GK_OK
+             : GK_ERR_CUDA;
+}
+
+gk_status gk_read_device_error(void* stream, uint32_t* bits, int clear) {
+  if (!bits) return GK_ERR_INVALID_ARG;
+  *bits = 0;
+  if (read_device_error(static_cast<cudaStream_t>(stream), bits, clear != 0) != cudaSuccess)
+    return GK_ERR_CUDA;
+  return *bits ? GK_ERR_DEVICE_BOUNDS : GK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,109 @@
+// gk_internal.h -- parameter blocks, workspace layout and launchers shared by
+// the host API (gk_api.cu) and the kernels (gk_kernels.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/gk.h"
+
+namespace gk {
+
+constexpr int kMaxGroups = 64;        // group buffers -> at most 128 layers
+constexpr int kHeadDim = 64;          // D
+constexpr int kGroup = 8;             // q heads per kv head (one MMA N tile)
+constexpr int kMaxBatch = 8192;
+constexpr int kStageTok = 32;         // tokens per pipeline stage
+constexpr int kStageKBytes = kStageTok * kHeadDim;   // 2 KB of K codes
+constexpr int kStageBytes = 2 * kStageKBytes;        // K + V
+constexpr int kMinSplit = 512;        // smallest split-KV chunk, tokens (power of two)
+constexpr int kMaxSplitsPerRow = 64;  // cap on chunks per (layer, row, kv head)
+constexpr int kPartialFloats = 2 * kGroup + kGroup * kHeadDim;  // m[8], l[8], o[8][64]
+
+// Header words at the start of the attention workspace.
+enum HdrWord {
+  kHdrQueue = 0,        // work counter (atomic)
+  kHdrNFull = 1,        // full-layer work units
+  kHdrNSwa = 2,         // sliding-window work units
+  kHdrNZero = 3,        // zero-fill units (inactive rows)
+  kHdrSplit = 4,        // split length in tokens
+  kHdrNEntries = 5,
+  kHdrTotalSplits = 6,
+  kHdrWords = 64
+};
+
+struct WsLayout {
+  size_t hdr, entries, swa_list, zero_list, ns, part_base, tickets, partials, total;
+  int64_t cap;          // partial records per (layer pair, kv head) plane
+  int64_t max_entries;
+};
+
+// Offsets for a workspace of `ws_bytes` (0 -> the recommended size).
+WsLayout ws_layout(const gk_shape& s, size_t ws_bytes);
+
+struct AppendParams {
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const float* cosb;
+  const float* sinb;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* upd_full;
+  const int32_t* upd_swa;
+  const uint8_t* active;
+  uint8_t* kb[kMaxGroups];
+  uint8_t* vb[kMaxGroups];
+  int NL, Bt, Hkv, B, nb;
+};
+
+struct PlanParams {
+  const int32_t* pos;
+  const uint8_t* active;
+  int32_t* hdr;
+  int32_t* entries;
+  int32_t* swa_list;
+  int32_t* zero_list;
+  int32_t* ns;
+  int32_t* part_base;
+  int32_t* tickets;
+  int64_t cap;
+  int NL, Bt, Hkv, n_warps;
+};
+
+struct AttnParams {
+  const uint16_t* q;
+  uint16_t* out;
+  float* out_f32;
+  const uint8_t* kb[kMaxGroups];
+  const uint8_t* vb[kMaxGroups];
+  const float* k_scale;
+  const float* v_scale;
+  const float* cosb;
+  const float* sinb;
+  const int32_t* bt_full;
+  const int32_t* bt_swa;
+  const int32_t* pos;
+  const int32_t* pos_w;
+  const int32_t* hdr;
+  int32_t* queue;
+  const int32_t* entries;
+  const int32_t* swa_list;
+  const int32_t* zero_list;
+  const int32_t* ns;
+  const int32_t* part_base;
+  int32_t* tickets;
+  float* partials;
+  int64_t cap;  // partial records per (layer pair, kv head) plane
+  int NL, Bt, Hq, Hkv, B, nb, W, MBF, MBS;
+};
+
+// Launchers (gk_kernels.cu).  They return the launch status.
+cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
+cudaError_t launch_quantize(const float* x, float scale, uint8_t* codes, int64_t n, cudaStream_t st);
+cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaStream_t st);
+// Resident warps of the persistent attention grid on the current device.
+int attention_resident_warps();
+cudaError_t read_device_error(cudaStream_t st, uint32_t* bits, bool clear);
+
+}  // namespace gk

@@ -1,0 +1,869 @@
+// gk_kernels.cu -- sm_103a kernels of the stack-wide paged-FP8 decode step.
+//
+//   kv_append_kernel   RoPE(k) in IEEE fp32, / scale, E4M3 (RNE, satfinite),
+//                      scatter into the packed K and plain V layouts.
+//   plan_kernel        one CTA: split-KV chunk length, work-unit order
+//                      (largest first), per-row split bookkeeping.
+//   attn_kernel        persistent: each warp takes (layer, row, kv head, split)
+//                      units from an atomic counter, streams 32-token stages of
+//                      K and V through a private ring of 1-D bulk copies, and
+//                      runs QK^T and PV on the tensor cores (mma.sync m16n8k16,
+//                      N = the 8 q heads of the GQA group) with an online
+//                      softmax.  Split units write (m, l, o) partials; the last
+//                      of a row's splits to finish merges them.
+//
+// Page references: "GPT-OSS-120B giga-kernel decode", sections "Kernel
+// contract" (layer parity i % 2 selects table / index / position, buffer
+// i / 2) and "KV-cache layout" (packed K view [.., block/2, d, 2], plain V).
+#include <cuda_runtime.h>
+
+#include "gk_device.cuh"
+#include "gk_internal.h"
+
+namespace gk {
+
+__device__ uint32_t g_dev_error;
+
+__device__ __forceinline__ void set_error(uint32_t bits) { atomicOr(&g_dev_error, bits); }
+
+// =========================================================================
+// KV append
+// =========================================================================
+// One warp per (layer i, row b, kv head h).  Lane l rotates the pair
+// (l, l + 32) of k and converts channels 2l, 2l + 1 of v.
+__global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ AppendParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t total = int64_t(p.NL) * p.Bt * p.Hkv;
+  if (row >= total) return;
+  const int h = int(row % p.Hkv);
+  const int64_t ib = row / p.Hkv;
+  const int b = int(ib % p.Bt);
+  const int i = int(ib / p.Bt);
+  if (!p.active[b]) return;
+  // layer parity: even = sliding window (upd_swa), odd = full (upd_full)
+  const int32_t slot = (i & 1) ? p.upd_full[b] : p.upd_swa[b];
+  if (slot < 0 || int64_t(slot) >= int64_t(p.nb) * p.B) {
+    if (lane == 0) set_error(GK_DEVERR_SLOT);
+    return;
+  }
+  const int64_t pb = slot / p.B;
+  const int t = slot % p.B;
+  const uint16_t* kr = p.k_new + row * kHeadDim;
+  const uint16_t* vr = p.v_new + row * kHeadDim;
+
+  const float x = __uint_as_float(uint32_t(kr[lane]) << 16);
+  const float y = __uint_as_float(uint32_t(kr[lane + 32]) << 16);
+  const float c = p.cosb[b * (kHeadDim / 2) + lane];
+  const float s = p.sinb[b * (kHeadDim / 2) + lane];
+  // fixed fp32 sequence, every operation rounded on its own (no contraction)
+  const float xr = __fsub_rn(__fmul_rn(x, c), __fmul_rn(y, s));
+  const float yr = __fadd_rn(__fmul_rn(y, c), __fmul_rn(x, s));
+  const float ks = p.k_scale[i];
+  const uint32_t kc = f32x2_to_e4m3x2(__fdiv_rn(xr, ks), __fdiv_rn(yr, ks));
+  // packed K: tokens 2p and 2p+1 interleaved per channel
+  uint8_t* kdst =
+      p.kb[i >> 1] + ((pb * p.Hkv + h) * (p.B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1);
+  kdst[2 * lane] = uint8_t(kc & 0xffu);
+  kdst[2 * (lane + 32)] = uint8_t(kc >> 8);
+
+  const uint32_t vw = reinterpret_cast<const uint32_t*>(vr)[lane];
+  const float vs = p.v_scale[i];
+  const uint32_t vc =
+      f32x2_to_e4m3x2(__fdiv_rn(bf16lo_to_f32(vw), vs), __fdiv_rn(bf16hi_to_f32(vw), vs));
+  uint8_t* vdst = p.vb[i >> 1] + ((pb * p.Hkv + h) * p.B + t) * kHeadDim;
+  reinterpret_cast<uint16_t*>(vdst)[lane] = uint16_t(vc);
+}
+
+__global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ x, float scale,
+                                                       uint8_t* __restrict__ codes, int64_t n) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x * 2;
+  for (int64_t i = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 2; i < n; i += stride) {
+    if (i + 1 < n) {
+      const uint32_t c = f32x2_to_e4m3x2(__fdiv_rn(x[i], scale), __fdiv_rn(x[i + 1], scale));
+      codes[i] = uint8_t(c & 0xffu);
+      codes[i + 1] = uint8_t(c >> 8);
+    } else {
+      codes[i] = uint8_t(f32x2_to_e4m3x2(__fdiv_rn(x[i], scale), 0.f) & 0xffu);
+    }
+  }
+}
+
+// =========================================================================
+// Planner (one CTA of 1024 threads)
+// =========================================================================
+constexpr int kPlanThreads = 1024;
+constexpr int kUnitsPerWarp = 4;
+constexpr int kSortMax = 2048;
+
+__device__ int64_t block_sum64(int64_t v, int64_t* red) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  __syncthreads();
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int64_t x = lane < nw ? red[lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    if (lane == 0) red[0] = x;
+  }
+  __syncthreads();
+  const int64_t r = red[0];
+  __syncthreads();
+  return r;
+}
+
+__device__ int block_max(int v, int* red) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(kFull, v, o));
+  __syncthreads();
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int x = lane < nw ? red[lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = max(x, __shfl_xor_sync(kFull, x, o));
+    if (lane == 0) red[0] = x;
+  }
+  __syncthreads();
+  const int r = red[0];
+  __syncthreads();
+  return r;
+}
+
+// Exclusive scan of one int per thread; *total gets the block sum.
+__device__ int block_excl_scan(int v, int* red, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) red[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int s = lane < nw ? red[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, s, o);
+      if (lane >= o) s += y;
+    }
+    red[lane] = s;
+  }
+  __syncthreads();
+  const int base = w > 0 ? red[w - 1] : 0;
+  *total = red[nw - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams p,
+                                                            int max_tokens_full) {
+  extern __shared__ int32_t plan_sm[];
+  int32_t* Ls = plan_sm;        // clamped context length per row (0 = no work)
+  int32_t* rem = plan_sm + p.Bt;
+  __shared__ int64_t red64[32];
+  __shared__ int red[32];
+  const int tid = threadIdx.x;
+  const int chunk = (p.Bt + blockDim.x - 1) / blockDim.x;
+  const int b_lo = min(p.Bt, tid * chunk), b_hi = min(p.Bt, b_lo + chunk);
+
+  int64_t tsum = 0;
+  int lmax = 0;
+  for (int b = b_lo; b < b_hi; ++b) {
+    int L = 0;
+    if (p.active[b]) {
+      const int pos = p.pos[b];
+      if (pos < 0) {
+        set_error(GK_DEVERR_POS);
+      } else {
+        L = pos + 1;
+        if (L > max_tokens_full) {
+          set_error(GK_DEVERR_POS);
+          L = max_tokens_full;
+        }
+      }
+    }
+    Ls[b] = L;
+    tsum += L;
+    lmax = max(lmax, L);
+  }
+  const int64_t T = block_sum64(tsum, red64);
+  const int Lmax = block_max(lmax, red);
+  const int planes = (p.NL >> 1) * p.Hkv;
+
+  // split length: a power of two >= kMinSplit giving about kUnitsPerWarp
+  // full-layer units per resident warp, at most kMaxSplitsPerRow chunks per
+  // row, and no more partial records than the workspace holds.
+  const int64_t s_bal = (T * planes) / (int64_t(max(1, p.n_warps)) * kUnitsPerWarp);
+  int64_t S = kMinSplit;
+  while (S < s_bal && S < (int64_t(1) << 30)) S <<= 1;
+  while (S * kMaxSplitsPerRow < Lmax) S <<= 1;
+  for (;;) {
+    int64_t need = 0;
+    for (int b = b_lo; b < b_hi; ++b)
+      if (Ls[b] > S) need += (Ls[b] + S - 1) / S;
+    need = block_sum64(need, red64);
+    if (need <= p.cap || S >= (int64_t(1) << 30)) break;
+    S <<= 1;
+  }
+
+  int n_full = 0, n_rem = 0, n_split = 0, n_act = 0, n_inact = 0;
+  for (int b = b_lo; b < b_hi; ++b) {
+    const int L = Ls[b];
+    if (L > 0) {
+      const int nf = int(L / S), r = int(L % S), ns = nf + (r > 0);
+      rem[b] = r;
+      p.ns[b] = ns;
+      n_full += nf;
+      n_rem += (r > 0);
+      n_split += ns > 1 ? ns : 0;
+      ++n_act;
+    } else {
+      rem[b] = 0;
+      p.ns[b] = 0;
+      ++n_inact;
+    }
+  }
+  int A, R, TS, NA, NI;
+  int fp = block_excl_scan(n_full, red, &A);       // also syncs rem[] writes
+  int rp = block_excl_scan(n_rem, red, &R);
+  int sp = block_excl_scan(n_split, red, &TS);
+  int ap = block_excl_scan(n_act, red, &NA);
+  int ip = block_excl_scan(n_inact, red, &NI);
+
+  for (int b = b_lo; b < b_hi; ++b) {
+    const int L = Ls[b];
+    if (L > 0) {
+      const int nf = int(L / S), r = rem[b], ns = nf + (r > 0);
+      for (int s = 0; s < nf; ++s) p.entries[fp++] = b | (s << 16);
+      if (r > 0) {
+        int rank;
+        if (p.Bt <= kSortMax) {  // remainders largest first, ties by row
+          rank = 0;
+          for (int c = 0; c < p.Bt; ++c) rank += (rem[c] > r) || (rem[c] == r && c < b);
+        } else {
+          rank = rp++;
+        }
+        p.entries[A + rank] = b | (nf << 16);
+      }
+      if (ns > 1) {
+        p.part_base[b] = sp;
+        sp += ns;
+        for (int j = 0; j < (p.NL >> 1); ++j)
+          for (int h = 0; h < p.Hkv; ++h) p.tickets[(int64_t(j) * p.Bt + b) * p.Hkv + h] = 0;
+      } else {
+        p.part_base[b] = 0;
+      }
+      p.swa_list[ap++] = b;
+    } else {
+      p.part_base[b] = 0;
+      p.zero_list[ip++] = b;
+    }
+  }
+  if (tid == 0) {
+    if (TS > p.cap) set_error(GK_DEVERR_PLAN);
+    p.hdr[kHdrQueue] = 0;
+    p.hdr[kHdrNFull] = (A + R) * planes;
+    p.hdr[kHdrNSwa] = NA * planes;
+    p.hdr[kHdrNZero] = NI * p.NL;
+    p.hdr[kHdrSplit] = int(S);
+    p.hdr[kHdrNEntries] = A + R;
+    p.hdr[kHdrTotalSplits] = TS;
+  }
+}
+
+// =========================================================================
+// Decode attention (persistent)
+// =========================================================================
+constexpr int kWarps = 4;    // independent worker warps per CTA
+constexpr int kStages = 4;   // ring depth per warp (stages of 32 tokens)
+constexpr int kFifo = 8;     // unit descriptors in flight per warp (> kStages + 1)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per barrier wait
+
+struct UnitDesc {
+  int32_t kind;  // 1 = full layer, 2 = sliding-window layer
+  int32_t layer, b, kvh, s, ns;
+  int32_t t_begin, t_end;  // key range [t_begin, t_end) in the table's frame
+  int32_t st_begin, n_st;  // 32-token stages covering the range
+};
+
+struct WarpSmem {
+  uint8_t ring[kStages][kStageBytes];
+  unsigned long long bar[kStages];
+  UnitDesc fifo[kFifo];
+};
+
+constexpr size_t kAttnSmem = sizeof(WarpSmem) * kWarps;
+
+__device__ __forceinline__ void zero_row(const AttnParams& p, int layer, int b, int lane) {
+  const int64_t base = (int64_t(layer) * p.Bt + b) * p.Hq * kHeadDim;
+  uint4* o = reinterpret_cast<uint4*>(p.out + base);
+  const int n16 = p.Hq * kHeadDim * 2 / 16;
+  for (int c = lane; c < n16; c += 32) o[c] = make_uint4(0, 0, 0, 0);
+  if (p.out_f32) {
+    float4* of = reinterpret_cast<float4*>(p.out_f32 + base);
+    for (int c = lane; c < 2 * n16; c += 32) of[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// Take the next unit from the global counter (warp-uniform).  Zero-fill units
+// (inactive rows) are done here.  Returns false when the queue is empty.
+__device__ __forceinline__ bool fetch_unit(const AttnParams& p, int lane, int nF, int nS, int nZ,
+                                           int S, int planes, UnitDesc& d) {
+  for (;;) {
+    int u = 0;
+    if (lane == 0) u = atomicAdd(p.queue, 1);
+    u = __shfl_sync(kFull, u, 0);
+    if (u < nF) {
+      const int e = u / planes, pl = u - e * planes;
+      const int j = pl / p.Hkv;
+      const int ent = p.entries[e];
+      const int b = ent & 0xffff, s = ent >> 16;
+      const int L = min(p.pos[b] + 1, p.MBF * p.B);
+      d.kind = 1;
+      d.layer = 2 * j + 1;
+      d.b = b;
+      d.kvh = pl - j * p.Hkv;
+      d.s = s;
+      d.ns = p.ns[b];
+      d.t_begin = s * S;
+      d.t_end = min(L, d.t_begin + S);
+    } else if (u < nF + nS) {
+      const int v = u - nF;
+      const int e = v / planes, pl = v - e * planes;
+      const int j = pl / p.Hkv;
+      const int b = p.swa_list[e];
+      int pw = p.pos_w[b];
+      if (pw < 0 || pw >= p.MBS * p.B) {
+        if (lane == 0) set_error(GK_DEVERR_POS);
+        pw = min(max(pw, 0), p.MBS * p.B - 1);
+      }
+      d.kind = 2;
+      d.layer = 2 * j;
+      d.b = b;
+      d.kvh = pl - j * p.Hkv;
+      d.s = 0;
+      d.ns = 1;
+      d.t_begin = max(0, pw - p.W + 1);
+      d.t_end = pw + 1;
+    } else if (u < nF + nS + nZ) {
+      const int v = u - nF - nS;
+      zero_row(p, v % p.NL, p.zero_list[v / p.NL], lane);
+      continue;
+    } else {
+      return false;
+    }
+    d.st_begin = d.t_begin / kStageTok;
+    d.n_st = (d.t_end + kStageTok - 1) / kStageTok - d.st_begin;
+    return true;
+  }
+}
+
+__global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, qd = lane & 3;
+  WarpSmem& ws = reinterpret_cast<WarpSmem*>(smem_raw)[warp];
+  const uint32_t ring0 = smem_u32(&ws.ring[0][0]);
+  const uint32_t bar0 = smem_u32(&ws.bar[0]);
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+
+  const int nF = p.hdr[kHdrNFull], nS = p.hdr[kHdrNSwa], nZ = p.hdr[kHdrNZero];
+  const int S = p.hdr[kHdrSplit];
+  const int planes = (p.NL >> 1) * p.Hkv;
+
+  // ------------------------------------------------ producer state
+  int prod = 0, cons = 0;
+  int f_head = 0, f_tail = 0;
+  bool exhausted = false;
+  int pk = 0, pu_n_st = 0, pu_st_begin = 0, pu_layer = 0, pu_b = 0, pu_kvh = 0, pu_kind = 0,
+      pu_t_end = 0;
+  int tbl_base = -1;
+  int32_t tbl = 0;
+  bool failed = false;
+
+  auto issue_next = [&]() -> bool {
+    if (exhausted) return false;
+    if (pk == pu_n_st) {
+      UnitDesc d;
+      if (!fetch_unit(p, lane, nF, nS, nZ, S, planes, d)) {
+        exhausted = true;
+        return false;
+      }
+      if (lane == 0) ws.fifo[f_tail % kFifo] = d;
+      __syncwarp();
+      ++f_tail;
+      pk = 0;
+      pu_n_st = d.n_st;
+      pu_st_begin = d.st_begin;
+      pu_layer = d.layer;
+      pu_b = d.b;
+      pu_kvh = d.kvh;
+      pu_kind = d.kind;
+      pu_t_end = d.t_end;
+      tbl_base = -1;
+    }
+    const int tok0 = (pu_st_begin + pk) * kStageTok;
+    const int slot = prod % kStages;
+    const uint32_t dst = ring0 + slot * kStageBytes;
+    const uint32_t bar = bar0 + 8 * slot;
+    const int32_t* row = pu_kind == 1 ? p.bt_full + int64_t(pu_b) * p.MBF
+                                      : p.bt_swa + int64_t(pu_b) * p.MBS;
+    const int row_len = pu_kind == 1 ? p.MBF : p.MBS;
+    const uint8_t* kbase = p.kb[pu_layer >> 1];
+    const uint8_t* vbase = p.vb[pu_layer >> 1];
+    const int B = p.B;
+    const int blk = tok0 / B;
+    const int nblk = B >= kStageTok ? 1 : 2;
+    if (tbl_base < 0 || blk + nblk - 1 >= tbl_base + 32) {
+      tbl_base = blk;
+      const int idx = blk + lane;
+      tbl = idx < row_len ? row[idx] : 0;
+    }
+    if (B >= kStageTok) {
+      int32_t pb = __shfl_sync(kFull, tbl, blk - tbl_base);
+      if (pb < 0 || pb >= p.nb) {
+        if (lane == 0) set_error(GK_DEVERR_BLOCK);
+        pb = 0;
+      }
+      if (lane == 0) {
+        const int64_t off = ((int64_t(pb) * p.Hkv + pu_kvh) * B + (tok0 - blk * B)) * kHeadDim;
+        mbar_arrive_expect_tx(bar, kStageBytes);
+        bulk_g2s(dst, kbase + off, kStageKBytes, bar);
+        bulk_g2s(dst + kStageKBytes, vbase + off, kStageKBytes, bar);
+      }
+    } else {  // 16-token blocks: two per stage
+      int32_t pb0 = __shfl_sync(kFull, tbl, blk - tbl_base);
+      int32_t pb1 = __shfl_sync(kFull, tbl, min(blk + 1 - tbl_base, 31));
+      const bool has1 = tok0 + B < pu_t_end;
+      if (pb0 < 0 || pb0 >= p.nb) {
+        if (lane == 0) set_error(GK_DEVERR_BLOCK);
+        pb0 = 0;
+      }
+      if (has1 && (blk + 1 >= row_len || pb1 < 0 || pb1 >= p.nb)) {
+        if (lane == 0) set_error(GK_DEVERR_BLOCK);
+        pb1 = 0;
+      }
+      if (lane == 0) {
+        const uint32_t half = uint32_t(B) * kHeadDim;
+        mbar_arrive_expect_tx(bar, has1 ? 4 * half : 2 * half);
+        const int64_t o0 = (int64_t(pb0) * p.Hkv + pu_kvh) * B * kHeadDim;
+        bulk_g2s(dst, kbase + o0, half, bar);
+        bulk_g2s(dst + kStageKBytes, vbase + o0, half, bar);
+        if (has1) {
+          const int64_t o1 = (int64_t(pb1) * p.Hkv + pu_kvh) * B * kHeadDim;
+          bulk_g2s(dst + half, kbase + o1, half, bar);
+          bulk_g2s(dst + kStageKBytes + half, vbase + o1, half, bar);
+        }
+      }
+    }
+    ++pk;
+    ++prod;
+    return true;
+  };
+
+  // ------------------------------------------------ consumer state
+  UnitDesc cd;
+  int k_in_unit = 0;
+  uint32_t qreg[8];
+  float cf0 = 0.f, cf1 = 0.f, m0 = 0.f, m1 = 0.f, l0 = 0.f, l1 = 0.f, vscale = 0.f;
+  float o[4][4];
+
+  while (prod - cons < kStages && issue_next()) {
+  }
+
+  while (cons < prod) {
+    if (k_in_unit == 0) {
+      cd = ws.fifo[f_head % kFifo];
+      // ---- unit prologue: rotated q for head (kvh*8 + g), channels 16qd..16qd+15
+      const int head = cd.kvh * kGroup + g;
+      const uint16_t* qrow =
+          p.q + ((int64_t(cd.layer) * p.Bt + cd.b) * p.Hq + head) * kHeadDim;
+      const uint4 x0 = *reinterpret_cast<const uint4*>(qrow + 16 * qd);
+      const uint4 x1 = *reinterpret_cast<const uint4*>(qrow + 16 * qd + 8);
+      const uint4 y0 = *reinterpret_cast<const uint4*>(qrow + 16 * (qd ^ 2));
+      const uint4 y1 = *reinterpret_cast<const uint4*>(qrow + 16 * (qd ^ 2) + 8);
+      const float* cp = p.cosb + cd.b * (kHeadDim / 2) + 16 * (qd & 1);
+      const float* sp = p.sinb + cd.b * (kHeadDim / 2) + 16 * (qd & 1);
+      const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const uint32_t yw[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+      const float sgn = qd < 2 ? -1.f : 1.f;
+      float r[16];
+      float amax = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const float2 cc = *reinterpret_cast<const float2*>(cp + 2 * w);
+        const float2 ss = *reinterpret_cast<const float2*>(sp + 2 * w);
+        r[2 * w] = bf16lo_to_f32(xw[w]) * cc.x + sgn * bf16lo_to_f32(yw[w]) * ss.x;
+        r[2 * w + 1] = bf16hi_to_f32(xw[w]) * cc.y + sgn * bf16hi_to_f32(yw[w]) * ss.y;
+        amax = fmaxf(amax, fmaxf(fabsf(r[2 * w]), fabsf(r[2 * w + 1])));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+      // power-of-two normalisation of the head so that max |q'| < 2^14 in f16
+      int ex = int((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+      ex = amax > 0.f ? min(max(ex, -100), 100) : 13;
+      const float f = __uint_as_float(uint32_t(127 + 13 - ex) << 23);
+      const float finv = __uint_as_float(uint32_t(127 - 13 + ex) << 23);
+#pragma unroll
+      for (int w = 0; w < 8; ++w) qreg[w] = f32x2_to_f16x2(r[2 * w] * f, r[2 * w + 1] * f);
+      // logits in log2 units: s * k_scale / sqrt(D) * log2(e), undoing f
+      const float cf = p.k_scale[cd.layer] * (0.125f * 1.4426950408889634f) * finv;
+      cf0 = __shfl_sync(kFull, cf, 8 * qd);
+      cf1 = __shfl_sync(kFull, cf, 8 * qd + 4);
+      vscale = p.v_scale[cd.layer];
+      m0 = m1 = -INFINITY;
+      l0 = l1 = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
+    }
+
+    // ---- wait for the stage
+    const int slot = cons % kStages;
+    const uint32_t bar = bar0 + 8 * slot;
+    const uint32_t parity = uint32_t(cons / kStages) & 1u;
+    if (!mbar_wait_bounded(bar, parity, kWaitLimitNs)) failed = true;
+    if (__any_sync(kFull, failed)) {
+      failed = true;
+      break;
+    }
+
+    const uint32_t Ks = ring0 + slot * kStageBytes;
+    const uint32_t Vs = Ks + kStageKBytes;
+    const int tok0 = (cd.st_begin + k_in_unit) * kStageTok;
+    const bool edge = tok0 < cd.t_begin || tok0 + kStageTok > cd.t_end;
+
+    // ---- S = q' K^T for two 16-token tiles; rows (g, g+8) = tokens (2p, 2p+1)
+    float sc[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+      const uint32_t kp = Ks + (8 * i + g) * (2 * kHeadDim) + 32 * qd;
+      const uint4 w0 = lds128(kp);
+      const uint4 w1 = lds128(kp + 16);
+      const uint32_t kw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x2x2(prmt(kw[2 * j], 0u, 0x3120u), a0, a1);
+        e4m3x4_to_f16x2x2(prmt(kw[2 * j + 1], 0u, 0x3120u), a2, a3);
+        mma_f16(sc[i], a0, a1, a2, a3, qreg[2 * j], qreg[2 * j + 1]);
+      }
+    }
+    // ---- online softmax (log2 domain); lane holds heads 2qd (c0,c2), 2qd+1 (c1,c3)
+    float xs[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      xs[i][0] = sc[i][0] * cf0;
+      xs[i][1] = sc[i][1] * cf1;
+      xs[i][2] = sc[i][2] * cf0;
+      xs[i][3] = sc[i][3] * cf1;
+    }
+    if (edge) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int t0 = tok0 + 16 * i + 2 * g;
+        if (t0 < cd.t_begin || t0 >= cd.t_end) xs[i][0] = xs[i][1] = -INFINITY;
+        if (t0 + 1 < cd.t_begin || t0 + 1 >= cd.t_end) xs[i][2] = xs[i][3] = -INFINITY;
+      }
+    }
+    float mx0 = fmaxf(fmaxf(xs[0][0], xs[0][2]), fmaxf(xs[1][0], xs[1][2]));
+    float mx1 = fmaxf(fmaxf(xs[0][1], xs[0][3]), fmaxf(xs[1][1], xs[1][3]));
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    float pr[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      pr[i][0] = ex2(xs[i][0] - mn0);
+      pr[i][1] = ex2(xs[i][1] - mn1);
+      pr[i][2] = ex2(xs[i][2] - mn0);
+      pr[i][3] = ex2(xs[i][3] - mn1);
+    }
+    l0 = l0 * al0 + ((pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]));
+    l1 = l1 * al1 + ((pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]));
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      o[m][0] *= al0;
+      o[m][2] *= al0;
+      o[m][1] *= al1;
+      o[m][3] *= al1;
+    }
+    // ---- O += P V; rows (g, g+8) = channels (8g+2m, 8g+2m+1), k = tokens 4qd..4qd+3
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t b0 = movmatrix_trans(f32x2_to_f16x2(pr[i][0], pr[i][1]));
+      const uint32_t b1 = movmatrix_trans(f32x2_to_f16x2(pr[i][2], pr[i][3]));
+      const uint32_t vp = Vs + (16 * i + 4 * qd) * kHeadDim + 8 * g;
+      uint2 v[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) v[r] = lds64(vp + r * kHeadDim);
+      if (edge) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int t = tok0 + 16 * i + 4 * qd + r;
+          if (t < cd.t_begin || t >= cd.t_end) v[r] = make_uint2(0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint32_t sel = (m & 1) ? 0x7362u : 0x5140u;
+        const uint32_t e02 = prmt(m < 2 ? v[0].x : v[0].y, m < 2 ? v[2].x : v[2].y, sel);
+        const uint32_t e13 = prmt(m < 2 ? v[1].x : v[1].y, m < 2 ? v[3].x : v[3].y, sel);
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x2x2(e02, a0, a1);
+        e4m3x4_to_f16x2x2(e13, a2, a3);
+        mma_f16(o[m], a0, a1, a2, a3, b0, b1);
+      }
+    }
+    __syncwarp();
+    ++cons;
+    ++k_in_unit;
+    while (prod - cons < kStages && issue_next()) {
+    }
+
+    if (k_in_unit == cd.n_st) {
+      // ---- unit epilogue
+      k_in_unit = 0;
+      ++f_head;
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(kFull, l0, off);
+        l1 += __shfl_xor_sync(kFull, l1, off);
+      }
+      const int64_t out_row =
+          ((int64_t(cd.layer) * p.Bt + cd.b) * p.Hq + cd.kvh * kGroup + 2 * qd) * kHeadDim + 8 * g;
+      if (cd.ns == 1) {
+        const float i0 = vscale / l0, i1 = vscale / l1;
+        float r0[8], r1[8];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          r0[2 * m] = o[m][0] * i0;
+          r0[2 * m + 1] = o[m][2] * i0;
+          r1[2 * m] = o[m][1] * i1;
+          r1[2 * m + 1] = o[m][3] * i1;
+        }
+        uint4 u0, u1;
+        u0.x = f32x2_to_bf16x2(r0[0], r0[1]);
+        u0.y = f32x2_to_bf16x2(r0[2], r0[3]);
+        u0.z = f32x2_to_bf16x2(r0[4], r0[5]);
+        u0.w = f32x2_to_bf16x2(r0[6], r0[7]);
+        u1.x = f32x2_to_bf16x2(r1[0], r1[1]);
+        u1.y = f32x2_to_bf16x2(r1[2], r1[3]);
+        u1.z = f32x2_to_bf16x2(r1[4], r1[5]);
+        u1.w = f32x2_to_bf16x2(r1[6], r1[7]);
+        *reinterpret_cast<uint4*>(p.out + out_row) = u0;
+        *reinterpret_cast<uint4*>(p.out + out_row + kHeadDim) = u1;
+        if (p.out_f32) {
+          float4* f0 = reinterpret_cast<float4*>(p.out_f32 + out_row);
+          float4* f1 = reinterpret_cast<float4*>(p.out_f32 + out_row + kHeadDim);
+          f0[0] = make_float4(r0[0], r0[1], r0[2], r0[3]);
+          f0[1] = make_float4(r0[4], r0[5], r0[6], r0[7]);
+          f1[0] = make_float4(r1[0], r1[1], r1[2], r1[3]);
+          f1[1] = make_float4(r1[4], r1[5], r1[6], r1[7]);
+        }
+      } else {
+        // split partial: (m, l, o) unnormalised, in log2 units
+        const int j = cd.layer >> 1;
+        const int64_t plane = int64_t(j) * p.Hkv + cd.kvh;
+        const int64_t cap = p.cap;
+        float* rec = p.partials + ((plane * cap) + p.part_base[cd.b] + cd.s) * kPartialFloats;
+        if (g == 0) {
+          rec[2 * qd] = m0;
+          rec[2 * qd + 1] = m1;
+          rec[kGroup + 2 * qd] = l0;
+          rec[kGroup + 2 * qd + 1] = l1;
+        }
+        float4* ro0 = reinterpret_cast<float4*>(rec + 2 * kGroup + (2 * qd) * kHeadDim + 8 * g);
+        float4* ro1 = reinterpret_cast<float4*>(rec + 2 * kGroup + (2 * qd + 1) * kHeadDim + 8 * g);
+        ro0[0] = make_float4(o[0][0], o[0][2], o[1][0], o[1][2]);
+        ro0[1] = make_float4(o[2][0], o[2][2], o[3][0], o[3][2]);
+        ro1[0] = make_float4(o[0][1], o[0][3], o[1][1], o[1][3]);
+        ro1[1] = make_float4(o[2][1], o[2][3], o[3][1], o[3][3]);
+        __threadfence();
+        __syncwarp();
+        int old = 0;
+        int32_t* ticket = p.tickets + (int64_t(j) * p.Bt + cd.b) * p.Hkv + cd.kvh;
+        if (lane == 0) old = atomicAdd(ticket, 1);
+        old = __shfl_sync(kFull, old, 0);
+        if (old == cd.ns - 1) {
+          // last split to finish: merge all of this row's partials in split order
+          __threadfence();
+          const float* base = p.partials + (plane * cap + p.part_base[cd.b]) * kPartialFloats;
+          float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
+          float a0[8], a1[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) a0[c] = a1[c] = 0.f;
+          for (int s = 0; s < cd.ns; ++s) {
+            const float* rs = base + int64_t(s) * kPartialFloats;
+            const float ms0 = ldg_cg_f(rs + 2 * qd), ms1 = ldg_cg_f(rs + 2 * qd + 1);
+            const float ls0 = ldg_cg_f(rs + kGroup + 2 * qd), ls1 = ldg_cg_f(rs + kGroup + 2 * qd + 1);
+            const float* os0 = rs + 2 * kGroup + (2 * qd) * kHeadDim + 8 * g;
+            const float* os1 = rs + 2 * kGroup + (2 * qd + 1) * kHeadDim + 8 * g;
+            const float4 p00 = ldg_cg_f4(os0), p01 = ldg_cg_f4(os0 + 4);
+            const float4 p10 = ldg_cg_f4(os1), p11 = ldg_cg_f4(os1 + 4);
+            const float n0 = fmaxf(M0, ms0), n1 = fmaxf(M1, ms1);
+            const float c0 = ex2(M0 - n0), w0 = ex2(ms0 - n0);
+            const float c1 = ex2(M1 - n1), w1 = ex2(ms1 - n1);
+            M0 = n0;
+            M1 = n1;
+            L0 = L0 * c0 + ls0 * w0;
+            L1 = L1 * c1 + ls1 * w1;
+            const float q0[8] = {p00.x, p00.y, p00.z, p00.w, p01.x, p01.y, p01.z, p01.w};
+            const float q1[8] = {p10.x, p10.y, p10.z, p10.w, p11.x, p11.y, p11.z, p11.w};
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              a0[c] = a0[c] * c0 + q0[c] * w0;
+              a1[c] = a1[c] * c1 + q1[c] * w1;
+            }
+          }
+          const float i0 = vscale / L0, i1 = vscale / L1;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            a0[c] *= i0;
+            a1[c] *= i1;
+          }
+          uint4 u0, u1;
+          u0.x = f32x2_to_bf16x2(a0[0], a0[1]);
+          u0.y = f32x2_to_bf16x2(a0[2], a0[3]);
+          u0.z = f32x2_to_bf16x2(a0[4], a0[5]);
+          u0.w = f32x2_to_bf16x2(a0[6], a0[7]);
+          u1.x = f32x2_to_bf16x2(a1[0], a1[1]);
+          u1.y = f32x2_to_bf16x2(a1[2], a1[3]);
+          u1.z = f32x2_to_bf16x2(a1[4], a1[5]);
+          u1.w = f32x2_to_bf16x2(a1[6], a1[7]);
+          *reinterpret_cast<uint4*>(p.out + out_row) = u0;
+          *reinterpret_cast<uint4*>(p.out + out_row + kHeadDim) = u1;
+          if (p.out_f32) {
+            float4* f0 = reinterpret_cast<float4*>(p.out_f32 + out_row);
+            float4* f1 = reinterpret_cast<float4*>(p.out_f32 + out_row + kHeadDim);
+            f0[0] = make_float4(a0[0], a0[1], a0[2], a0[3]);
+            f0[1] = make_float4(a0[4], a0[5], a0[6], a0[7]);
+            f1[0] = make_float4(a1[0], a1[1], a1[2], a1[3]);
+            f1[1] = make_float4(a1[4], a1[5], a1[6], a1[7]);
+          }
+        }
+      }
+    }
+  }
+
+  if (failed) {
+    // A barrier wait hit its limit: record it, then wait (bounded) for this
+    // warp's copies still in flight before the CTA may exit.
+    if (lane == 0) set_error(GK_DEVERR_TIMEOUT);
+    for (int c = cons; c < prod; ++c) {
+      const uint32_t bar = bar0 + 8 * (c % kStages);
+      const uint32_t parity = uint32_t(c / kStages) & 1u;
+      mbar_wait_bounded(bar, parity, kWaitLimitNs);
+    }
+  }
+}
+
+// =========================================================================
+// Launchers
+// =========================================================================
+struct DeviceCache {
+  int dev = -1;
+  int sms = 0;
+  int attn_blocks_per_sm = 0;
+  bool attrs_set = false;
+};
+static DeviceCache g_cache[64];
+
+static cudaError_t device_setup(DeviceCache** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  DeviceCache& c = g_cache[dev];
+  if (!c.attrs_set) {
+    e = cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kAttnSmem));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(2 * kMaxBatch * sizeof(int32_t)));
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.attn_blocks_per_sm, attn_kernel,
+                                                      kWarps * 32, kAttnSmem);
+    if (e != cudaSuccess) return e;
+    if (c.attn_blocks_per_sm < 1) c.attn_blocks_per_sm = 1;
+    c.dev = dev;
+    c.attrs_set = true;
+  }
+  *out = &c;
+  return cudaSuccess;
+}
+
+int attention_resident_warps() {
+  DeviceCache* c = nullptr;
+  if (device_setup(&c) != cudaSuccess) return 0;
+  return c->sms * c->attn_blocks_per_sm * kWarps;
+}
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t st) {
+  const int64_t warps = int64_t(p.NL) * p.Bt * p.Hkv;
+  if (warps == 0) return cudaSuccess;
+  const int threads = 256;
+  const int64_t blocks = (warps * 32 + threads - 1) / threads;
+  kv_append_kernel<<<unsigned(blocks), threads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const float* x, float scale, uint8_t* codes, int64_t n,
+                            cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  DeviceCache* c = nullptr;
+  cudaError_t e = device_setup(&c);
+  if (e != cudaSuccess) return e;
+  const int threads = 256;
+  int64_t blocks = (n / 2 + threads) / threads;
+  blocks = blocks < int64_t(c->sms) * 8 ? blocks : int64_t(c->sms) * 8;
+  quantize_kernel<<<unsigned(blocks), threads, 0, st>>>(x, scale, codes, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaStream_t st) {
+  DeviceCache* c = nullptr;
+  cudaError_t e = device_setup(&c);
+  if (e != cudaSuccess) return e;
+  PlanParams pp = plan;
+  pp.n_warps = c->sms * c->attn_blocks_per_sm * kWarps;
+  plan_kernel<<<1, kPlanThreads, size_t(2) * p.Bt * sizeof(int32_t), st>>>(pp, p.MBF * p.B);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  attn_kernel<<<c->sms * c->attn_blocks_per_sm, kWarps * 32, kAttnSmem, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t read_device_error(cudaStream_t st, uint32_t* bits, bool clear) {
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(bits, g_dev_error, sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
+  if (clear) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(uint32_t));
+  }
+  return e;
+}
+
+}  // namespace gk

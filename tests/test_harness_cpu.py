@@ -1,0 +1,46 @@
+"""CPU checks of the test harness itself: the compact-pool helpers used for the
+full-size sampled parity checks give exactly what the whole-step oracle gives."""
+import numpy as np
+import pytest
+
+import gk_inputs as gi
+import gk_testlib as tl
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged_small", "block16_small"])
+def test_row_pair_sampler_equals_whole_step(name):
+    w = gi.get(name)
+    c = gi.make_control(w)
+    st = gi.make_step(w, "cpu")
+    cache = gi.make_cache(w, c, "cpu")
+    full, _, _ = tl.oracle_step(w, c, st, cache)
+    host = {k: gi.bf16_bits(v) for k, v in st.items()}
+    G = w.num_q_heads // w.num_kv_heads
+    for b in range(w.batch):
+        if not c.active[b]:
+            continue
+        for j in range(w.num_layers // 2):
+            res = tl.oracle_row_pair(w, c, host, cache, j, b)
+            for (layer, kvh), o in res.items():
+                assert np.array_equal(o, full[layer, b, kvh * G:(kvh + 1) * G]), (b, layer, kvh)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged_small", "swa_small_sat"])
+def test_appended_codes_helper_equals_whole_buffer_append(name):
+    w = gi.get(name)
+    c = gi.make_control(w)
+    st = gi.make_step(w, "cpu")
+    cache = gi.make_cache(w, c, "cpu")
+    _, kb, vb = tl.oracle_step(w, c, st, cache)
+    kc, vc = tl.oracle_appended_codes(w, c, st)
+    B, Hkv, D = w.block_size, w.num_kv_heads, w.head_dim
+    for i in range(w.num_layers):
+        upd = c.upd_swa if i % 2 == 0 else c.upd_full
+        kview = kb[i // 2].reshape(c.num_blocks, Hkv, B // 2, D, 2)
+        vview = vb[i // 2].reshape(c.num_blocks, Hkv, B, D)
+        for b in range(w.batch):
+            if not c.active[b]:
+                continue
+            pb, t = divmod(int(upd[b]), B)
+            assert np.array_equal(kc[i, b], kview[pb, :, t // 2, :, t % 2])
+            assert np.array_equal(vc[i, b], vview[pb, :, t, :])
