@@ -24,7 +24,9 @@ Workload recipe (stated once, used everywhere):
   * physical block ids are one random permutation of [0, nb - 1) handed out in
     sequence order; nb = blocks used + 1 unless the workload fixes it;
   * cos/sin rows: angle pos_b * theta^(-2e/D), e < D/2, in double, stored fp32;
-  * q, k_new, v_new ~ N(0, sigma) drawn in fp32 and rounded to bf16;
+  * q ~ N(0, sigma_q), k_new and v_new ~ N(0, sigma), drawn in fp32 and
+    rounded to bf16 (the short-context workload's "KV values ~ N(0, 3)" is read
+    as sigma = 3 for K and V only; q stays N(0, 1));
   * cache bytes: codes of N(0, sigma_cache) / scale, drawn by torch and cast
     with torch's float8_e4m3fn conversion after clamping to +-448 (a library
     cast; the cache is an input like any other);
@@ -55,7 +57,8 @@ class Workload:
     head_dim: int = 64
     window: int = 128
     inactive_frac: float = 0.0
-    sigma: float = 1.0            # q, k_new, v_new
+    sigma: float = 1.0            # k_new, v_new
+    sigma_q: float = 1.0          # q
     sigma_cache: float = 1.0      # pre-filled cache values (before 1/scale)
     scale: Optional[float] = None  # None: per-layer 2^-(4 + i mod 3)
     theta: float = 150000.0
@@ -84,8 +87,8 @@ WORKLOADS = {
                                         "10% of rows inactive"),
     "swa_b512": Workload("swa_b512", 36, 512, 64, 8, 32, "uniform:64,512", seed=5, sigma=3.0,
                          sigma_cache=3.0, scale=1 / 16,
-                         description="36 layers, batch 512, L ~ U{64..512}, values N(0, 3), "
-                                     "scale 1/16"),
+                         description="36 layers, batch 512, L ~ U{64..512}, KV values N(0, 3), "
+                                     "q N(0, 1), scale 1/16"),
 }
 WORKLOADS["swa_b512_sat"] = WORKLOADS["swa_b512"].replace(
     name="swa_b512_sat", sat_probe=True,
@@ -105,6 +108,11 @@ REDUCED = {
         name="swa_small", num_layers=4, batch=16, lengths="uniform:64,512", seed=15),
     "swa_small_sat": WORKLOADS["swa_b512_sat"].replace(
         name="swa_small_sat", num_layers=4, batch=16, lengths="uniform:64,512", seed=16),
+    # stress variant, not one of the five workloads: q ~ N(0, 3) as well, so
+    # logits have a standard deviation near 9 and the softmax is very peaked
+    "swa_small_peaky": WORKLOADS["swa_b512"].replace(
+        name="swa_small_peaky", num_layers=4, batch=16, lengths="uniform:64,512", seed=18,
+        sigma_q=3.0),
     "block16_small": WORKLOADS["tiny"].replace(
         name="block16_small", num_layers=4, batch=5, num_q_heads=16, num_kv_heads=2,
         lengths="fixed:1,15,16,143,300", seed=17, num_blocks=None),
@@ -240,7 +248,7 @@ def make_step(w: Workload, device="cpu") -> dict:
     """q [NL,Bt,Hq,D], k_new and v_new [NL,Bt,Hkv,D]: bf16 torch tensors."""
     g = _gen(device, w.seed * 7919 + 1)
     NL, Bt, D = w.num_layers, w.batch, w.head_dim
-    q = (torch.randn(NL, Bt, w.num_q_heads, D, generator=g, device=device) * w.sigma).to(torch.bfloat16)
+    q = (torch.randn(NL, Bt, w.num_q_heads, D, generator=g, device=device) * w.sigma_q).to(torch.bfloat16)
     k = (torch.randn(NL, Bt, w.num_kv_heads, D, generator=g, device=device) * w.sigma)
     v = (torch.randn(NL, Bt, w.num_kv_heads, D, generator=g, device=device) * w.sigma)
     if w.sat_probe:

@@ -118,6 +118,20 @@ __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
   return d;
 }
 
+// f16x2 -> (lo, hi) fp32, exact.
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h) {
+  float2 r;
+  asm("{\n"
+      " .reg .b16 l, h;\n"
+      " mov.b32 {l, h}, %2;\n"
+      " cvt.f32.f16 %0, l;\n"
+      " cvt.f32.f16 %1, h;\n"
+      "}\n"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(h));
+  return r;
+}
+
 // (lo, hi) fp32 -> bf16x2 with lo in the low half; round to nearest even.
 __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
   uint32_t d;

@@ -285,6 +285,7 @@ constexpr int kWarps = 4;    // independent worker warps per CTA
 constexpr int kStages = 4;   // ring depth per warp (stages of 32 tokens)
 constexpr int kFifo = 8;     // unit descriptors in flight per warp (> kStages + 1)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per barrier wait
+constexpr uint32_t kOnesF16x2 = 0x3C003C00u;        // (1.0, 1.0) in f16
 
 struct UnitDesc {
   int32_t kind;  // 1 = full layer, 2 = sliding-window layer
@@ -476,9 +477,10 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
   // ------------------------------------------------ consumer state
   UnitDesc cd;
   int k_in_unit = 0;
-  uint32_t qreg[8];
-  float cf0 = 0.f, cf1 = 0.f, m0 = 0.f, m1 = 0.f, l0 = 0.f, l1 = 0.f, vscale = 0.f;
+  uint32_t qhi[8], qlo[8];  // q' = qhi + qlo (f16 each): ~22-bit significand
+  float cf0 = 0.f, cf1 = 0.f, m0 = 0.f, m1 = 0.f, vscale = 0.f;
   float o[4][4];
+  float lacc[4];  // softmax denominators from a ones-row MMA over the f16 P
 
   while (prod - cons < kStages && issue_next()) {
   }
@@ -517,14 +519,19 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
       const float f = __uint_as_float(uint32_t(127 + 13 - ex) << 23);
       const float finv = __uint_as_float(uint32_t(127 - 13 + ex) << 23);
 #pragma unroll
-      for (int w = 0; w < 8; ++w) qreg[w] = f32x2_to_f16x2(r[2 * w] * f, r[2 * w + 1] * f);
+      for (int w = 0; w < 8; ++w) {
+        const float a = r[2 * w] * f, b = r[2 * w + 1] * f;
+        qhi[w] = f32x2_to_f16x2(a, b);
+        const float2 h = f16x2_to_f32x2(qhi[w]);
+        qlo[w] = f32x2_to_f16x2(a - h.x, b - h.y);  // residual is exact in fp32
+      }
       // logits in log2 units: s * k_scale / sqrt(D) * log2(e), undoing f
       const float cf = p.k_scale[cd.layer] * (0.125f * 1.4426950408889634f) * finv;
       cf0 = __shfl_sync(kFull, cf, 8 * qd);
       cf1 = __shfl_sync(kFull, cf, 8 * qd + 4);
       vscale = p.v_scale[cd.layer];
       m0 = m1 = -INFINITY;
-      l0 = l1 = 0.f;
+      lacc[0] = lacc[1] = lacc[2] = lacc[3] = 0.f;
 #pragma unroll
       for (int m = 0; m < 4; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
     }
@@ -558,7 +565,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
         uint32_t a0, a1, a2, a3;
         e4m3x4_to_f16x2x2(prmt(kw[2 * j], 0u, 0x3120u), a0, a1);
         e4m3x4_to_f16x2x2(prmt(kw[2 * j + 1], 0u, 0x3120u), a2, a3);
-        mma_f16(sc[i], a0, a1, a2, a3, qreg[2 * j], qreg[2 * j + 1]);
+        mma_f16(sc[i], a0, a1, a2, a3, qlo[2 * j], qlo[2 * j + 1]);
+        mma_f16(sc[i], a0, a1, a2, a3, qhi[2 * j], qhi[2 * j + 1]);
       }
     }
     // ---- online softmax (log2 domain); lane holds heads 2qd (c0,c2), 2qd+1 (c1,c3)
@@ -597,8 +605,10 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
       pr[i][2] = ex2(xs[i][2] - mn0);
       pr[i][3] = ex2(xs[i][3] - mn1);
     }
-    l0 = l0 * al0 + ((pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]));
-    l1 = l1 * al1 + ((pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]));
+    lacc[0] *= al0;
+    lacc[2] *= al0;
+    lacc[1] *= al1;
+    lacc[3] *= al1;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       o[m][0] *= al0;
@@ -611,6 +621,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
     for (int i = 0; i < 2; ++i) {
       const uint32_t b0 = movmatrix_trans(f32x2_to_f16x2(pr[i][0], pr[i][1]));
       const uint32_t b1 = movmatrix_trans(f32x2_to_f16x2(pr[i][2], pr[i][3]));
+      // every row of the ones matrix sums the same rounded P the values see
+      mma_f16(lacc, kOnesF16x2, kOnesF16x2, kOnesF16x2, kOnesF16x2, b0, b1);
       const uint32_t vp = Vs + (16 * i + 4 * qd) * kHeadDim + 8 * g;
       uint2 v[4];
 #pragma unroll
@@ -643,11 +655,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
       // ---- unit epilogue
       k_in_unit = 0;
       ++f_head;
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(kFull, l0, off);
-        l1 += __shfl_xor_sync(kFull, l1, off);
-      }
+      const float l0 = lacc[0], l1 = lacc[1];
       const int64_t out_row =
           ((int64_t(cd.layer) * p.Bt + cd.b) * p.Hq + cd.kvh * kGroup + 2 * qd) * kHeadDim + 8 * g;
       if (cd.ns == 1) {

@@ -45,6 +45,7 @@ def check_out(out_bf16: np.ndarray, out_f32, ref: np.ndarray, what: str = ""):
         assert e.max() <= MAX_ABS, (what, "f32 max", float(e.max()))
         assert e.mean() <= MEAN_ABS, (what, "f32 mean", float(e.mean()))
         stats.update(f32_max=float(e.max()), f32_mean=float(e.mean()))
+    print("check_out", what, {k: round(v, 6) for k, v in stats.items()})
     return stats
 
 
