@@ -18,8 +18,9 @@
  *   - All tensor pointers are DEVICE pointers unless a parameter says "host".
  *   - The caller owns every buffer.  The library allocates nothing, keeps no
  *     state between calls other than a per-device error word (see
- *     gk_read_device_error) and cached device properties, and does not retain
- *     pointers after a call returns.
+ *     gk_read_device_error), cached device properties and the fixed scratch
+ *     array of gk_decode_attn_stack_static, and does not retain pointers after
+ *     a call returns.
  *   - `stream` is a cudaStream_t passed as void*.  Calls are asynchronous and
  *     stream-ordered: a call returns after validating its arguments and
  *     enqueueing its kernels.  NULL means the legacy default stream.
@@ -143,6 +144,39 @@ gk_status gk_decode_attn_stack(const gk_shape *shape, const void *q, void *const
                                const int32_t *bt_swa, const int32_t *pos, const int32_t *pos_w,
                                const uint8_t *active, void *out, float *out_f32,
                                void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * gk_decode_attn_stack_static -- gk_decode_attn_stack without a caller
+ * workspace.  (No counterpart on the pages: an addition of this library.)
+ *
+ * For callers that cannot allocate device memory: a host framework that
+ * budgets every device byte before the first step, a plugin or foreign-language
+ * boundary with no device allocator, or a step that must not risk the
+ * synchronisation and failure modes of cudaMalloc.  The library holds a
+ * GK_STATIC_SCRATCH_BYTES device array of its own on every GPU that loads it,
+ * until the process exits; this call allocates nothing and uses that array as
+ * the workspace.  Arguments and results are those of gk_decode_attn_stack
+ * (the caller still passes inputs and outputs).
+ *   - Returns GK_ERR_WORKSPACE when the shape needs more than
+ *     GK_STATIC_SCRATCH_BYTES of workspace (gk_attn_workspace_min_bytes); a
+ *     smaller array than the recommended workspace only means fewer split-KV
+ *     chunks.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; each call re-initialises what it needs.  Calls that may overlap
+ *     on the GPU (different streams without ordering between them) race on the
+ *     array and give wrong results: order them.
+ */
+#define GK_STATIC_SCRATCH_BYTES (16u << 20)
+gk_status gk_decode_attn_stack_static(const gk_shape *shape, const void *q, void *const *k_bufs,
+                                      void *const *v_bufs, const float *k_scale,
+                                      const float *v_scale, const float *cos, const float *sin,
+                                      const int32_t *bt_full, const int32_t *bt_swa,
+                                      const int32_t *pos, const int32_t *pos_w,
+                                      const uint8_t *active, void *out, float *out_f32,
+                                      void *stream);
 
 /*
  * gk_e4m3_quantize -- codes[i] = E4M3(x[i] / scale) with the same fp32

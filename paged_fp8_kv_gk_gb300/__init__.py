@@ -6,6 +6,7 @@ is no CPU fallback: if the library cannot be built or loaded, or a tensor is not
 on a CUDA device, the calls raise.
 
 The functions carry the C names: ``gk_kv_append``, ``gk_decode_attn_stack``,
+``gk_decode_attn_stack_static``,
 ``gk_attn_workspace_bytes``, ``gk_attn_workspace_min_bytes``,
 ``gk_e4m3_quantize``, ``gk_read_device_error``, ``gk_status_str``,
 ``gk_abi_version``.  Tensors are torch tensors; the stream defaults to torch's
@@ -79,6 +80,8 @@ def lib(build_if_needed: bool = True) -> ctypes.CDLL:
             L.gk_attn_workspace_min_bytes.argtypes = [sp]
             L.gk_decode_attn_stack.restype = ctypes.c_int
             L.gk_decode_attn_stack.argtypes = [sp] + [vp] * 15 + [sz, vp]
+            L.gk_decode_attn_stack_static.restype = ctypes.c_int
+            L.gk_decode_attn_stack_static.argtypes = [sp] + [vp] * 15
             L.gk_e4m3_quantize.restype = ctypes.c_int
             L.gk_e4m3_quantize.argtypes = [vp, ctypes.c_float, vp, i64, vp]
             L.gk_read_device_error.restype = ctypes.c_int
@@ -181,6 +184,28 @@ def gk_decode_attn_stack(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, b
         _ptr(out_f32, torch.float32, "out_f32", allow_none=True),
         _ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()), _stream(stream, q))
     _check(st, "gk_decode_attn_stack")
+
+
+def gk_decode_attn_stack_static(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, bt_full,
+                                bt_swa, pos, pos_w, active, out, out_f32=None,
+                                stream=None) -> None:
+    """gk_decode_attn_stack without a caller workspace, for callers that cannot
+    allocate device memory: the library's own fixed scratch array
+    (GK_STATIC_SCRATCH_BYTES per GPU) serves as the workspace.  Calls on one
+    device share that array, so they must not overlap on the GPU."""
+    import torch
+    sh = _as_shape(shape)
+    st = lib().gk_decode_attn_stack_static(
+        ctypes.byref(sh), _ptr(q, torch.bfloat16, "q"),
+        ctypes.cast(_ptr_array(k_bufs, "k_bufs"), ctypes.c_void_p),
+        ctypes.cast(_ptr_array(v_bufs, "v_bufs"), ctypes.c_void_p),
+        _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
+        _ptr(cos, torch.float32, "cos"), _ptr(sin, torch.float32, "sin"),
+        _ptr(bt_full, torch.int32, "bt_full"), _ptr(bt_swa, torch.int32, "bt_swa"),
+        _ptr(pos, torch.int32, "pos"), _ptr(pos_w, torch.int32, "pos_w"),
+        _ptr(active, torch.uint8, "active"), _ptr(out, torch.bfloat16, "out"),
+        _ptr(out_f32, torch.float32, "out_f32", allow_none=True), _stream(stream, q))
+    _check(st, "gk_decode_attn_stack_static")
 
 
 def gk_e4m3_quantize(x, scale: float, codes, stream=None) -> None:
