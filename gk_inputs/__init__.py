@@ -119,11 +119,17 @@ REDUCED = {
 }
 
 
+# Profiling size of the 36-layer workload: same per-row shape, 8 rows, about
+# 0.7 GB of KV per step (larger than L2, small enough for a full counter set).
+PROFILE = {
+    "gptoss_b8": WORKLOADS["gptoss_b64"].replace(name="gptoss_b8", batch=8, seed=22),
+}
+
+
 def get(name: str) -> Workload:
-    if name in WORKLOADS:
-        return WORKLOADS[name]
-    if name in REDUCED:
-        return REDUCED[name]
+    for table in (WORKLOADS, REDUCED, PROFILE):
+        if name in table:
+            return table[name]
     raise KeyError(name)
 
 
