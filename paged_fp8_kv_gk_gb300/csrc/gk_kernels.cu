@@ -286,6 +286,7 @@ constexpr int kStages = 4;   // ring depth per warp (stages of 32 tokens)
 constexpr int kFifo = 8;     // unit descriptors in flight per warp (> kStages + 1)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per barrier wait
 constexpr uint32_t kOnesF16x2 = 0x3C003C00u;        // (1.0, 1.0) in f16
+constexpr float kLazyLog2 = 8.f;  // probabilities stay <= 2^8 between rescales
 
 struct UnitDesc {
   int32_t kind;  // 1 = full layer, 2 = sliding-window layer
@@ -478,7 +479,12 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
   UnitDesc cd;
   int k_in_unit = 0;
   uint32_t qhi[8], qlo[8];  // q' = qhi + qlo (f16 each): ~22-bit significand
-  float cf0 = 0.f, cf1 = 0.f, m0 = 0.f, m1 = 0.f, vscale = 0.f;
+  // Scores come out of the MMA as x * 2^e_h, x = logit in log2 units and
+  // 2^e_h the per-head normalisation of q; si_h = 2^-e_h undoes it.  mr_h is
+  // the running reference maximum (raw units), allowed to lag the true
+  // maximum by up to kLazyLog2 so that most stages skip the rescale.
+  float si0 = 0.f, si1 = 0.f, mr0 = 0.f, mr1 = 0.f, nb0 = 0.f, nb1 = 0.f, thr0 = 0.f,
+        thr1 = 0.f, vscale = 0.f;
   float o[4][4];
   float lacc[4];  // softmax denominators from a ones-row MMA over the f16 P
 
@@ -501,14 +507,16 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
       const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
       const uint32_t yw[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
       const float sgn = qd < 2 ? -1.f : 1.f;
+      // logits in log2 units: q'.k * k_scale / sqrt(D) * log2(e), folded into q
+      const float ck = p.k_scale[cd.layer] * (0.125f * 1.4426950408889634f);
       float r[16];
       float amax = 0.f;
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
         const float2 cc = *reinterpret_cast<const float2*>(cp + 2 * w);
         const float2 ss = *reinterpret_cast<const float2*>(sp + 2 * w);
-        r[2 * w] = bf16lo_to_f32(xw[w]) * cc.x + sgn * bf16lo_to_f32(yw[w]) * ss.x;
-        r[2 * w + 1] = bf16hi_to_f32(xw[w]) * cc.y + sgn * bf16hi_to_f32(yw[w]) * ss.y;
+        r[2 * w] = (bf16lo_to_f32(xw[w]) * cc.x + sgn * bf16lo_to_f32(yw[w]) * ss.x) * ck;
+        r[2 * w + 1] = (bf16hi_to_f32(xw[w]) * cc.y + sgn * bf16hi_to_f32(yw[w]) * ss.y) * ck;
         amax = fmaxf(amax, fmaxf(fabsf(r[2 * w]), fabsf(r[2 * w + 1])));
       }
       amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
@@ -525,12 +533,11 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
         const float2 h = f16x2_to_f32x2(qhi[w]);
         qlo[w] = f32x2_to_f16x2(a - h.x, b - h.y);  // residual is exact in fp32
       }
-      // logits in log2 units: s * k_scale / sqrt(D) * log2(e), undoing f
-      const float cf = p.k_scale[cd.layer] * (0.125f * 1.4426950408889634f) * finv;
-      cf0 = __shfl_sync(kFull, cf, 8 * qd);
-      cf1 = __shfl_sync(kFull, cf, 8 * qd + 4);
+      si0 = __shfl_sync(kFull, finv, 8 * qd);   // heads 2qd and 2qd+1
+      si1 = __shfl_sync(kFull, finv, 8 * qd + 4);
       vscale = p.v_scale[cd.layer];
-      m0 = m1 = -INFINITY;
+      mr0 = mr1 = thr0 = thr1 = -INFINITY;
+      nb0 = nb1 = 0.f;
       lacc[0] = lacc[1] = lacc[2] = lacc[3] = 0.f;
 #pragma unroll
       for (int m = 0; m < 4; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
@@ -570,51 +577,52 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
       }
     }
     // ---- online softmax (log2 domain); lane holds heads 2qd (c0,c2), 2qd+1 (c1,c3)
-    float xs[2][4];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      xs[i][0] = sc[i][0] * cf0;
-      xs[i][1] = sc[i][1] * cf1;
-      xs[i][2] = sc[i][2] * cf0;
-      xs[i][3] = sc[i][3] * cf1;
-    }
     if (edge) {
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int t0 = tok0 + 16 * i + 2 * g;
-        if (t0 < cd.t_begin || t0 >= cd.t_end) xs[i][0] = xs[i][1] = -INFINITY;
-        if (t0 + 1 < cd.t_begin || t0 + 1 >= cd.t_end) xs[i][2] = xs[i][3] = -INFINITY;
+        if (t0 < cd.t_begin || t0 >= cd.t_end) sc[i][0] = sc[i][1] = -INFINITY;
+        if (t0 + 1 < cd.t_begin || t0 + 1 >= cd.t_end) sc[i][2] = sc[i][3] = -INFINITY;
       }
     }
-    float mx0 = fmaxf(fmaxf(xs[0][0], xs[0][2]), fmaxf(xs[1][0], xs[1][2]));
-    float mx1 = fmaxf(fmaxf(xs[0][1], xs[0][3]), fmaxf(xs[1][1], xs[1][3]));
+    const float lm0 = fmaxf(fmaxf(sc[0][0], sc[0][2]), fmaxf(sc[1][0], sc[1][2]));
+    const float lm1 = fmaxf(fmaxf(sc[0][1], sc[0][3]), fmaxf(sc[1][1], sc[1][3]));
+    if (__any_sync(kFull, lm0 > thr0 || lm1 > thr1)) {
+      // some score passed its reference by more than 2^kLazyLog2: move the
+      // reference to the true running maximum and rescale what was summed
+      float w0 = lm0, w1 = lm1;
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+      for (int off = 4; off < 32; off <<= 1) {
+        w0 = fmaxf(w0, __shfl_xor_sync(kFull, w0, off));
+        w1 = fmaxf(w1, __shfl_xor_sync(kFull, w1, off));
+      }
+      const float n0 = fmaxf(mr0, w0), n1 = fmaxf(mr1, w1);
+      const float al0 = ex2((mr0 - n0) * si0), al1 = ex2((mr1 - n1) * si1);
+      mr0 = n0;
+      mr1 = n1;
+      nb0 = -n0 * si0;
+      nb1 = -n1 * si1;
+      thr0 = n0 + kLazyLog2 / si0;
+      thr1 = n1 + kLazyLog2 / si1;
+      lacc[0] *= al0;
+      lacc[2] *= al0;
+      lacc[1] *= al1;
+      lacc[3] *= al1;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        o[m][0] *= al0;
+        o[m][2] *= al0;
+        o[m][1] *= al1;
+        o[m][3] *= al1;
+      }
     }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
     float pr[2][4];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      pr[i][0] = ex2(xs[i][0] - mn0);
-      pr[i][1] = ex2(xs[i][1] - mn1);
-      pr[i][2] = ex2(xs[i][2] - mn0);
-      pr[i][3] = ex2(xs[i][3] - mn1);
-    }
-    lacc[0] *= al0;
-    lacc[2] *= al0;
-    lacc[1] *= al1;
-    lacc[3] *= al1;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      o[m][0] *= al0;
-      o[m][2] *= al0;
-      o[m][1] *= al1;
-      o[m][3] *= al1;
+      pr[i][0] = ex2(fmaf(sc[i][0], si0, nb0));
+      pr[i][1] = ex2(fmaf(sc[i][1], si1, nb1));
+      pr[i][2] = ex2(fmaf(sc[i][2], si0, nb0));
+      pr[i][3] = ex2(fmaf(sc[i][3], si1, nb1));
     }
     // ---- O += P V; rows (g, g+8) = channels (8g+2m, 8g+2m+1), k = tokens 4qd..4qd+3
 #pragma unroll
@@ -694,8 +702,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
         const int64_t cap = p.cap;
         float* rec = p.partials + ((plane * cap) + p.part_base[cd.b] + cd.s) * kPartialFloats;
         if (g == 0) {
-          rec[2 * qd] = m0;
-          rec[2 * qd + 1] = m1;
+          rec[2 * qd] = mr0 * si0;  // log2 units
+          rec[2 * qd + 1] = mr1 * si1;
           rec[kGroup + 2 * qd] = l0;
           rec[kGroup + 2 * qd + 1] = l1;
         }
