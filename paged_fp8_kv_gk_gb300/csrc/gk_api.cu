@@ -53,13 +53,9 @@ WsLayout ws_layout(const gk_shape& s, size_t ws_bytes) {
   const size_t after_hdr = off;
   auto place = [&](int64_t cap) {
     size_t o = after_hdr;
-    L.entries = o;
-    o = align256(o + size_t(s.batch + cap) * sizeof(int32_t));
-    L.swa_list = o;
-    o = align256(o + size_t(s.batch) * sizeof(int32_t));
+    L.edesc = o;  // full-layer entries (at most batch + cap), then one window entry per row
+    o = align256(o + size_t(2 * s.batch + cap) * sizeof(int4));
     L.zero_list = o;
-    o = align256(o + size_t(s.batch) * sizeof(int32_t));
-    L.ns = o;
     o = align256(o + size_t(s.batch) * sizeof(int32_t));
     L.part_base = o;
     o = align256(o + size_t(s.batch) * sizeof(int32_t));
@@ -79,7 +75,7 @@ WsLayout ws_layout(const gk_shape& s, size_t ws_bytes) {
   const size_t fixed = L.total;
   int64_t cap = 0;
   if (ws_bytes > fixed + 512) {
-    cap = int64_t((ws_bytes - fixed - 512) / (size_t(planes) * rec + sizeof(int32_t)));
+    cap = int64_t((ws_bytes - fixed - 512) / (size_t(planes) * rec + sizeof(int4)));
     const int64_t cmax = int64_t(s.batch) * kMaxSplitsPerRow;
     if (cap > cmax) cap = cmax;
   }
@@ -194,14 +190,10 @@ gk_status gk_decode_attn_stack(const gk_shape* shape, const void* q, void* const
   p.sinb = sin;
   p.bt_full = bt_full;
   p.bt_swa = bt_swa;
-  p.pos = pos;
-  p.pos_w = pos_w;
   p.hdr = reinterpret_cast<const int32_t*>(ws + L.hdr);
   p.queue = reinterpret_cast<int32_t*>(ws + L.hdr) + kHdrQueue;
-  p.entries = reinterpret_cast<const int32_t*>(ws + L.entries);
-  p.swa_list = reinterpret_cast<const int32_t*>(ws + L.swa_list);
+  p.edesc = reinterpret_cast<const int4*>(ws + L.edesc);
   p.zero_list = reinterpret_cast<const int32_t*>(ws + L.zero_list);
-  p.ns = reinterpret_cast<const int32_t*>(ws + L.ns);
   p.part_base = reinterpret_cast<const int32_t*>(ws + L.part_base);
   p.tickets = reinterpret_cast<int32_t*>(ws + L.tickets);
   p.partials = reinterpret_cast<float*>(ws + L.partials);
@@ -219,18 +211,20 @@ gk_status gk_decode_attn_stack(const gk_shape* shape, const void* q, void* const
   PlanParams pl;
   memset(&pl, 0, sizeof(pl));
   pl.pos = pos;
+  pl.pos_w = pos_w;
   pl.active = active;
   pl.hdr = reinterpret_cast<int32_t*>(ws + L.hdr);
-  pl.entries = reinterpret_cast<int32_t*>(ws + L.entries);
-  pl.swa_list = reinterpret_cast<int32_t*>(ws + L.swa_list);
+  pl.edesc = reinterpret_cast<int4*>(ws + L.edesc);
   pl.zero_list = reinterpret_cast<int32_t*>(ws + L.zero_list);
-  pl.ns = reinterpret_cast<int32_t*>(ws + L.ns);
   pl.part_base = reinterpret_cast<int32_t*>(ws + L.part_base);
   pl.tickets = reinterpret_cast<int32_t*>(ws + L.tickets);
   pl.cap = L.cap;
   pl.NL = shape->num_layers;
   pl.Bt = shape->batch;
   pl.Hkv = shape->num_kv_heads;
+  pl.W = shape->window;
+  pl.max_tokens_full = shape->max_blocks_full * shape->block_size;
+  pl.max_tokens_swa = shape->max_blocks_swa * shape->block_size;
   return launch_attention(pl, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GK_OK
                                                                                    : GK_ERR_CUDA;
 }

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <vector_types.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -24,8 +25,7 @@ constexpr int kPartialFloats = 2 * kGroup + kGroup * kHeadDim;  // m[8], l[8], o
 // Header words at the start of the attention workspace.
 enum HdrWord {
   kHdrQueue = 0,        // work counter (atomic)
-  kHdrNFull = 1,        // full-layer work units
-  kHdrNSwa = 2,         // sliding-window work units
+  kHdrNUnits = 1,       // units with a descriptor (full-layer, then sliding-window)
   kHdrNZero = 3,        // zero-fill units (inactive rows)
   kHdrSplit = 4,        // split length in tokens
   kHdrNEntries = 5,
@@ -34,7 +34,7 @@ enum HdrWord {
 };
 
 struct WsLayout {
-  size_t hdr, entries, swa_list, zero_list, ns, part_base, tickets, partials, total;
+  size_t hdr, edesc, zero_list, part_base, tickets, partials, total;
   int64_t cap;          // partial records per (layer pair, kv head) plane
   int64_t max_entries;
 };
@@ -59,16 +59,16 @@ struct AppendParams {
 
 struct PlanParams {
   const int32_t* pos;
+  const int32_t* pos_w;
   const uint8_t* active;
   int32_t* hdr;
-  int32_t* entries;
-  int32_t* swa_list;
+  int4* edesc;
   int32_t* zero_list;
-  int32_t* ns;
   int32_t* part_base;
   int32_t* tickets;
   int64_t cap;
-  int NL, Bt, Hkv, n_warps;
+  int NL, Bt, Hkv, W, n_warps;
+  int max_tokens_full, max_tokens_swa;  // table row lengths in tokens
 };
 
 struct AttnParams {
@@ -83,14 +83,10 @@ struct AttnParams {
   const float* sinb;
   const int32_t* bt_full;
   const int32_t* bt_swa;
-  const int32_t* pos;
-  const int32_t* pos_w;
   const int32_t* hdr;
   int32_t* queue;
-  const int32_t* entries;
-  const int32_t* swa_list;
+  const int4* edesc;
   const int32_t* zero_list;
-  const int32_t* ns;
   const int32_t* part_base;
   int32_t* tickets;
   float* partials;

@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__
 // Planner (one CTA of 1024 threads)
 // =========================================================================
 constexpr int kPlanThreads = 1024;
-constexpr int kUnitsPerWarp = 4;
+constexpr int kUnitsPerWarp = 8;   // minimum work units per resident warp
 constexpr int kSortMax = 2048;
 
 __device__ int64_t block_sum64(int64_t v, int64_t* red) {
@@ -162,8 +162,13 @@ __device__ int block_excl_scan(int v, int* red, int* total) {
   return base + x - v;
 }
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams p,
-                                                            int max_tokens_full) {
+// Work entries are int4 descriptors: {row b, t_begin, t_end, w} with
+// w = s | ns << 16 | kind << 30 (kind 1 = sliding-window layer).  One entry
+// covers the (layer pair, kv head) planes of one row's chunk: unit u is plane
+// u % planes of entry u / planes.  Full-layer entries come first, largest
+// first; then one sliding-window entry per active row; then zero-fill units
+// (one per inactive row and layer).
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams p) {
   extern __shared__ int32_t plan_sm[];
   int32_t* Ls = plan_sm;        // clamped context length per row (0 = no work)
   int32_t* rem = plan_sm + p.Bt;
@@ -174,7 +179,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   const int b_lo = min(p.Bt, tid * chunk), b_hi = min(p.Bt, b_lo + chunk);
 
   int64_t tsum = 0;
-  int lmax = 0;
+  int lmax = 0, nact = 0;
   for (int b = b_lo; b < b_hi; ++b) {
     int L = 0;
     if (p.active[b]) {
@@ -183,10 +188,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         set_error(GK_DEVERR_POS);
       } else {
         L = pos + 1;
-        if (L > max_tokens_full) {
+        if (L > p.max_tokens_full) {
           set_error(GK_DEVERR_POS);
-          L = max_tokens_full;
+          L = p.max_tokens_full;
         }
+        ++nact;
       }
     }
     Ls[b] = L;
@@ -195,14 +201,26 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   }
   const int64_t T = block_sum64(tsum, red64);
   const int Lmax = block_max(lmax, red);
+  const int64_t NAct = block_sum64(nact, red64);
   const int planes = (p.NL >> 1) * p.Hkv;
+  const int64_t warps = max(1, p.n_warps);
 
-  // split length: a power of two >= kMinSplit giving about kUnitsPerWarp
-  // full-layer units per resident warp, at most kMaxSplitsPerRow chunks per
-  // row, and no more partial records than the workspace holds.
-  const int64_t s_bal = (T * planes) / (int64_t(max(1, p.n_warps)) * kUnitsPerWarp);
+  // Split length S (a power of two >= kMinSplit).  Start near a quarter of
+  // one warp's share of the full-layer work, then halve while there are
+  // fewer than kUnitsPerWarp units per resident warp (uniform long rows need
+  // many chunks; mixed rows balance through largest-first order).  Then cap
+  // the chunks per row and fit the partial records into the workspace.
   int64_t S = kMinSplit;
-  while (S < s_bal && S < (int64_t(1) << 30)) S <<= 1;
+  const int64_t share = (T * planes) / (warps * 4);
+  while (S < share && S < (int64_t(1) << 30)) S <<= 1;
+  while (S > kMinSplit) {
+    int64_t units = 0;
+    for (int b = b_lo; b < b_hi; ++b)
+      if (Ls[b] > 0) units += (Ls[b] + S - 1) / S;
+    units = (block_sum64(units, red64) + NAct) * planes;
+    if (units >= kUnitsPerWarp * warps) break;
+    S >>= 1;
+  }
   while (S * kMaxSplitsPerRow < Lmax) S <<= 1;
   for (;;) {
     int64_t need = 0;
@@ -219,14 +237,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     if (L > 0) {
       const int nf = int(L / S), r = int(L % S), ns = nf + (r > 0);
       rem[b] = r;
-      p.ns[b] = ns;
       n_full += nf;
       n_rem += (r > 0);
       n_split += ns > 1 ? ns : 0;
       ++n_act;
     } else {
       rem[b] = 0;
-      p.ns[b] = 0;
       ++n_inact;
     }
   }
@@ -236,12 +252,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   int sp = block_excl_scan(n_split, red, &TS);
   int ap = block_excl_scan(n_act, red, &NA);
   int ip = block_excl_scan(n_inact, red, &NI);
+  const int NEF = A + R;  // full-layer entries
 
   for (int b = b_lo; b < b_hi; ++b) {
     const int L = Ls[b];
     if (L > 0) {
       const int nf = int(L / S), r = rem[b], ns = nf + (r > 0);
-      for (int s = 0; s < nf; ++s) p.entries[fp++] = b | (s << 16);
+      for (int s = 0; s < nf; ++s)
+        p.edesc[fp++] = make_int4(b, int(s * S), int((s + 1) * S), s | (ns << 16));
       if (r > 0) {
         int rank;
         if (p.Bt <= kSortMax) {  // remainders largest first, ties by row
@@ -250,7 +268,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         } else {
           rank = rp++;
         }
-        p.entries[A + rank] = b | (nf << 16);
+        p.edesc[A + rank] = make_int4(b, int(nf * S), L, nf | (ns << 16));
       }
       if (ns > 1) {
         p.part_base[b] = sp;
@@ -260,7 +278,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
       } else {
         p.part_base[b] = 0;
       }
-      p.swa_list[ap++] = b;
+      // sliding-window layer of this row: keys [max(0, pos_w - W + 1), pos_w]
+      int pw = p.pos_w[b];
+      if (pw < 0 || pw >= p.max_tokens_swa) {
+        set_error(GK_DEVERR_POS);
+        pw = min(max(pw, 0), p.max_tokens_swa - 1);
+      }
+      p.edesc[NEF + ap++] = make_int4(b, max(0, pw - p.W + 1), pw + 1, (1 << 16) | (1 << 30));
     } else {
       p.part_base[b] = 0;
       p.zero_list[ip++] = b;
@@ -269,11 +293,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   if (tid == 0) {
     if (TS > p.cap) set_error(GK_DEVERR_PLAN);
     p.hdr[kHdrQueue] = 0;
-    p.hdr[kHdrNFull] = (A + R) * planes;
-    p.hdr[kHdrNSwa] = NA * planes;
+    p.hdr[kHdrNUnits] = (NEF + NA) * planes;
     p.hdr[kHdrNZero] = NI * p.NL;
     p.hdr[kHdrSplit] = int(S);
-    p.hdr[kHdrNEntries] = A + R;
+    p.hdr[kHdrNEntries] = NEF + NA;
     p.hdr[kHdrTotalSplits] = TS;
   }
 }
@@ -282,8 +305,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
 // Decode attention (persistent)
 // =========================================================================
 constexpr int kWarps = 4;    // independent worker warps per CTA
-constexpr int kStages = 4;   // ring depth per warp (stages of 32 tokens)
-constexpr int kFifo = 8;     // unit descriptors in flight per warp (> kStages + 1)
+constexpr int kStages = 3;   // ring depth per warp (stages of 32 tokens)
+constexpr int kFifo = 6;     // unit descriptors in flight per warp (> kStages + 1)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per barrier wait
 constexpr uint32_t kOnesF16x2 = 0x3C003C00u;        // (1.0, 1.0) in f16
 constexpr float kLazyLog2 = 8.f;  // probabilities stay <= 2^8 between rescales
@@ -295,11 +318,23 @@ struct UnitDesc {
   int32_t st_begin, n_st;  // 32-token stages covering the range
 };
 
-struct WarpSmem {
+// q of the unit's 8 heads (bf16) followed by its row's cos and sin (fp32),
+// fetched with the unit's first stage.
+constexpr uint32_t kQBytes = kGroup * kHeadDim * 2;
+constexpr uint32_t kRopeBytes = (kHeadDim / 2) * 4;
+constexpr uint32_t kUnitHeadBytes = kQBytes + 2 * kRopeBytes;
+
+// One per warp, laid out back to back: the 128-byte alignment keeps every
+// warp's ring and q buffer on the 16-byte boundary bulk copies require.
+struct alignas(128) WarpSmem {
   uint8_t ring[kStages][kStageBytes];
+  uint8_t qbuf[kUnitHeadBytes];
   unsigned long long bar[kStages];
   UnitDesc fifo[kFifo];
 };
+static_assert(sizeof(WarpSmem) % 128 == 0, "warp areas must stay 128-byte aligned");
+static_assert(kStageBytes % 16 == 0 && kUnitHeadBytes % 16 == 0 && kStageKBytes % 16 == 0,
+              "bulk-copy destinations must be 16-byte aligned");
 
 constexpr size_t kAttnSmem = sizeof(WarpSmem) * kWarps;
 
@@ -314,65 +349,33 @@ __device__ __forceinline__ void zero_row(const AttnParams& p, int layer, int b, 
   }
 }
 
-// Take the next unit from the global counter (warp-uniform).  Zero-fill units
-// (inactive rows) are done here.  Returns false when the queue is empty.
-__device__ __forceinline__ bool fetch_unit(const AttnParams& p, int lane, int nF, int nS, int nZ,
-                                           int S, int planes, UnitDesc& d) {
-  for (;;) {
-    int u = 0;
-    if (lane == 0) u = atomicAdd(p.queue, 1);
-    u = __shfl_sync(kFull, u, 0);
-    if (u < nF) {
-      const int e = u / planes, pl = u - e * planes;
-      const int j = pl / p.Hkv;
-      const int ent = p.entries[e];
-      const int b = ent & 0xffff, s = ent >> 16;
-      const int L = min(p.pos[b] + 1, p.MBF * p.B);
-      d.kind = 1;
-      d.layer = 2 * j + 1;
-      d.b = b;
-      d.kvh = pl - j * p.Hkv;
-      d.s = s;
-      d.ns = p.ns[b];
-      d.t_begin = s * S;
-      d.t_end = min(L, d.t_begin + S);
-    } else if (u < nF + nS) {
-      const int v = u - nF;
-      const int e = v / planes, pl = v - e * planes;
-      const int j = pl / p.Hkv;
-      const int b = p.swa_list[e];
-      int pw = p.pos_w[b];
-      if (pw < 0 || pw >= p.MBS * p.B) {
-        if (lane == 0) set_error(GK_DEVERR_POS);
-        pw = min(max(pw, 0), p.MBS * p.B - 1);
-      }
-      d.kind = 2;
-      d.layer = 2 * j;
-      d.b = b;
-      d.kvh = pl - j * p.Hkv;
-      d.s = 0;
-      d.ns = 1;
-      d.t_begin = max(0, pw - p.W + 1);
-      d.t_end = pw + 1;
-    } else if (u < nF + nS + nZ) {
-      const int v = u - nF - nS;
-      zero_row(p, v % p.NL, p.zero_list[v / p.NL], lane);
-      continue;
-    } else {
-      return false;
-    }
-    d.st_begin = d.t_begin / kStageTok;
-    d.n_st = (d.t_end + kStageTok - 1) / kStageTok - d.st_begin;
-    return true;
-  }
+// Unit u covers plane u % planes of work entry e = u / planes.
+__device__ __forceinline__ void decode_unit(const AttnParams& p, int u, int4 e, int planes,
+                                            UnitDesc& d) {
+  const int pl = u - (u / planes) * planes;
+  const int j = pl / p.Hkv;
+  const bool swa = ((e.w >> 30) & 1) != 0;
+  d.kind = swa ? 2 : 1;
+  d.layer = swa ? 2 * j : 2 * j + 1;
+  d.b = e.x;
+  d.kvh = pl - j * p.Hkv;
+  d.s = e.w & 0xffff;
+  d.ns = (e.w >> 16) & 0x3fff;
+  d.t_begin = e.y;
+  d.t_end = e.z;
+  d.st_begin = e.y / kStageTok;
+  d.n_st = (e.z + kStageTok - 1) / kStageTok - d.st_begin;
 }
 
-__global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_constant__ AttnParams p) {
+// 4 CTAs (16 warps) per SM: latency hiding across warps measured worth more
+// than a deeper ring or the registers above 128.
+__global__ void __launch_bounds__(kWarps * 32, 4) attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, qd = lane & 3;
   WarpSmem& ws = reinterpret_cast<WarpSmem*>(smem_raw)[warp];
   const uint32_t ring0 = smem_u32(&ws.ring[0][0]);
+  const uint32_t qbuf0 = smem_u32(&ws.qbuf[0]);
   const uint32_t bar0 = smem_u32(&ws.bar[0]);
   if (lane == 0) {
 #pragma unroll
@@ -381,9 +384,31 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
   }
   __syncwarp();
 
-  const int nF = p.hdr[kHdrNFull], nS = p.hdr[kHdrNSwa], nZ = p.hdr[kHdrNZero];
-  const int S = p.hdr[kHdrSplit];
+  const int nU = p.hdr[kHdrNUnits], nZ = p.hdr[kHdrNZero];
   const int planes = (p.NL >> 1) * p.Hkv;
+
+  // ------------------------------------------------ scheduler pipeline
+  // Each warp holds one claimed unit ahead of the one it streams: its
+  // descriptor is loaded when it is claimed and its first block-table chunk
+  // while the current unit streams.  (Claiming two ahead measured slower.)
+  int u_after = 0, u_next = 0;
+  if (lane == 0) {
+    u_next = atomicAdd(p.queue, 1);
+  }
+  u_next = __shfl_sync(kFull, u_next, 0);
+  int4 e_next = u_next < nU ? p.edesc[u_next / planes] : make_int4(0, 0, 0, 0);
+  bool tn_ready = false;
+  int32_t tbl_next = 0;
+  int tbl_next_base = 0;
+  // lane l: entry l of the table chunk starting at the unit's first block
+  auto load_tbl = [&](int4 e, int& base) -> int32_t {
+    const bool swa = ((e.w >> 30) & 1) != 0;
+    const int32_t* row = swa ? p.bt_swa + int64_t(e.x) * p.MBS : p.bt_full + int64_t(e.x) * p.MBF;
+    const int row_len = swa ? p.MBS : p.MBF;
+    base = ((e.y / kStageTok) * kStageTok) / p.B;
+    const int idx = base + lane;
+    return idx < row_len ? __ldg(row + idx) : 0;
+  };
 
   // ------------------------------------------------ producer state
   int prod = 0, cons = 0;
@@ -394,12 +419,56 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
   int tbl_base = -1;
   int32_t tbl = 0;
   bool failed = false;
+  bool q_free = true;  // the q buffer may take the next unit's q
+
+  // lane 0: copy the producer unit's q (8 heads) and its row's cos/sin rows
+  auto issue_unit_head = [&](uint32_t bar) {
+    const uint16_t* qsrc =
+        p.q + ((int64_t(pu_layer) * p.Bt + pu_b) * p.Hq + int64_t(pu_kvh) * kGroup) * kHeadDim;
+    bulk_g2s(qbuf0, qsrc, kQBytes, bar);
+    bulk_g2s(qbuf0 + kQBytes, p.cosb + int64_t(pu_b) * (kHeadDim / 2), kRopeBytes, bar);
+    bulk_g2s(qbuf0 + kQBytes + kRopeBytes, p.sinb + int64_t(pu_b) * (kHeadDim / 2), kRopeBytes, bar);
+  };
+
+  // Next unit from the pipeline (warp-uniform); zero-fill units (inactive
+  // rows) are done here.  Returns false when the queue is empty.
+  auto next_unit = [&](UnitDesc& d) -> bool {
+    for (;;) {
+      const int u = u_next;
+      const int4 e = e_next;
+      if (u >= nU + nZ) return false;
+      int32_t tcur = 0;
+      int tcur_base = 0;
+      if (u < nU) {
+        if (tn_ready) {
+          tcur = tbl_next;
+          tcur_base = tbl_next_base;
+        } else {
+          tcur = load_tbl(e, tcur_base);
+        }
+      }
+      if (lane == 0) u_after = atomicAdd(p.queue, 1);
+      u_next = __shfl_sync(kFull, u_after, 0);
+      e_next = u_next < nU ? p.edesc[u_next / planes] : make_int4(0, 0, 0, 0);
+      tn_ready = false;
+      if (u >= nU) {
+        const int v = u - nU;
+        zero_row(p, v % p.NL, p.zero_list[v / p.NL], lane);
+        continue;
+      }
+      decode_unit(p, u, e, planes, d);
+      tbl = tcur;
+      tbl_base = tcur_base;
+      return true;
+    }
+  };
 
   auto issue_next = [&]() -> bool {
     if (exhausted) return false;
     if (pk == pu_n_st) {
+      if (!q_free) return false;  // the consumer has not read the buffered q yet
       UnitDesc d;
-      if (!fetch_unit(p, lane, nF, nS, nZ, S, planes, d)) {
+      if (!next_unit(d)) {
         exhausted = true;
         return false;
       }
@@ -414,8 +483,12 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
       pu_kvh = d.kvh;
       pu_kind = d.kind;
       pu_t_end = d.t_end;
-      tbl_base = -1;
+      q_free = false;
+    } else if (!tn_ready && u_next < nU) {
+      tbl_next = load_tbl(e_next, tbl_next_base);
+      tn_ready = true;
     }
+    const uint32_t head_bytes = pk == 0 ? kUnitHeadBytes : 0u;
     const int tok0 = (pu_st_begin + pk) * kStageTok;
     const int slot = prod % kStages;
     const uint32_t dst = ring0 + slot * kStageBytes;
@@ -441,7 +514,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
       }
       if (lane == 0) {
         const int64_t off = ((int64_t(pb) * p.Hkv + pu_kvh) * B + (tok0 - blk * B)) * kHeadDim;
-        mbar_arrive_expect_tx(bar, kStageBytes);
+        mbar_arrive_expect_tx(bar, kStageBytes + head_bytes);
+        if (head_bytes) issue_unit_head(bar);
         bulk_g2s(dst, kbase + off, kStageKBytes, bar);
         bulk_g2s(dst + kStageKBytes, vbase + off, kStageKBytes, bar);
       }
@@ -459,7 +533,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
       }
       if (lane == 0) {
         const uint32_t half = uint32_t(B) * kHeadDim;
-        mbar_arrive_expect_tx(bar, has1 ? 4 * half : 2 * half);
+        mbar_arrive_expect_tx(bar, (has1 ? 4 * half : 2 * half) + head_bytes);
+        if (head_bytes) issue_unit_head(bar);
         const int64_t o0 = (int64_t(pb0) * p.Hkv + pu_kvh) * B * kHeadDim;
         bulk_g2s(dst, kbase + o0, half, bar);
         bulk_g2s(dst + kStageKBytes, vbase + o0, half, bar);
@@ -492,20 +567,37 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
   }
 
   while (cons < prod) {
+    // ---- wait for the stage (the unit's first stage also brings its q)
+    const int slot = cons % kStages;
+    const uint32_t bar = bar0 + 8 * slot;
+    const uint32_t parity = uint32_t(cons / kStages) & 1u;
+    if (!mbar_wait_bounded(bar, parity, kWaitLimitNs)) failed = true;
+    if (__any_sync(kFull, failed)) {
+      failed = true;
+      break;
+    }
     if (k_in_unit == 0) {
       cd = ws.fifo[f_head % kFifo];
       // ---- unit prologue: rotated q for head (kvh*8 + g), channels 16qd..16qd+15
-      const int head = cd.kvh * kGroup + g;
-      const uint16_t* qrow =
-          p.q + ((int64_t(cd.layer) * p.Bt + cd.b) * p.Hq + head) * kHeadDim;
-      const uint4 x0 = *reinterpret_cast<const uint4*>(qrow + 16 * qd);
-      const uint4 x1 = *reinterpret_cast<const uint4*>(qrow + 16 * qd + 8);
-      const uint4 y0 = *reinterpret_cast<const uint4*>(qrow + 16 * (qd ^ 2));
-      const uint4 y1 = *reinterpret_cast<const uint4*>(qrow + 16 * (qd ^ 2) + 8);
-      const float* cp = p.cosb + cd.b * (kHeadDim / 2) + 16 * (qd & 1);
-      const float* sp = p.sinb + cd.b * (kHeadDim / 2) + 16 * (qd & 1);
+      const uint32_t qrow = qbuf0 + g * (kHeadDim * 2);
+      const uint4 x0 = lds128(qrow + 32 * qd);
+      const uint4 x1 = lds128(qrow + 32 * qd + 16);
+      const uint4 y0 = lds128(qrow + 32 * (qd ^ 2));
+      const uint4 y1 = lds128(qrow + 32 * (qd ^ 2) + 16);
+      const uint32_t cp = qbuf0 + kQBytes + 64 * (qd & 1);
+      const uint32_t sp = cp + kRopeBytes;
       const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
       const uint32_t yw[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+      uint32_t cw[16], sw[16];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 c4 = lds128(cp + 16 * k);
+        const uint4 s4 = lds128(sp + 16 * k);
+        cw[4 * k] = c4.x; cw[4 * k + 1] = c4.y; cw[4 * k + 2] = c4.z; cw[4 * k + 3] = c4.w;
+        sw[4 * k] = s4.x; sw[4 * k + 1] = s4.y; sw[4 * k + 2] = s4.z; sw[4 * k + 3] = s4.w;
+      }
+      __syncwarp();
+      q_free = true;
       const float sgn = qd < 2 ? -1.f : 1.f;
       // logits in log2 units: q'.k * k_scale / sqrt(D) * log2(e), folded into q
       const float ck = p.k_scale[cd.layer] * (0.125f * 1.4426950408889634f);
@@ -513,10 +605,10 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
       float amax = 0.f;
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
-        const float2 cc = *reinterpret_cast<const float2*>(cp + 2 * w);
-        const float2 ss = *reinterpret_cast<const float2*>(sp + 2 * w);
-        r[2 * w] = (bf16lo_to_f32(xw[w]) * cc.x + sgn * bf16lo_to_f32(yw[w]) * ss.x) * ck;
-        r[2 * w + 1] = (bf16hi_to_f32(xw[w]) * cc.y + sgn * bf16hi_to_f32(yw[w]) * ss.y) * ck;
+        const float c0 = __uint_as_float(cw[2 * w]), c1 = __uint_as_float(cw[2 * w + 1]);
+        const float s0 = __uint_as_float(sw[2 * w]), s1 = __uint_as_float(sw[2 * w + 1]);
+        r[2 * w] = (bf16lo_to_f32(xw[w]) * c0 + sgn * bf16lo_to_f32(yw[w]) * s0) * ck;
+        r[2 * w + 1] = (bf16hi_to_f32(xw[w]) * c1 + sgn * bf16hi_to_f32(yw[w]) * s1) * ck;
         amax = fmaxf(amax, fmaxf(fabsf(r[2 * w]), fabsf(r[2 * w + 1])));
       }
       amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
@@ -541,16 +633,6 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attn_kernel(const __grid_const
       lacc[0] = lacc[1] = lacc[2] = lacc[3] = 0.f;
 #pragma unroll
       for (int m = 0; m < 4; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
-    }
-
-    // ---- wait for the stage
-    const int slot = cons % kStages;
-    const uint32_t bar = bar0 + 8 * slot;
-    const uint32_t parity = uint32_t(cons / kStages) & 1u;
-    if (!mbar_wait_bounded(bar, parity, kWaitLimitNs)) failed = true;
-    if (__any_sync(kFull, failed)) {
-      failed = true;
-      break;
     }
 
     const uint32_t Ks = ring0 + slot * kStageBytes;
@@ -863,7 +945,7 @@ cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaSt
   if (e != cudaSuccess) return e;
   PlanParams pp = plan;
   pp.n_warps = c->sms * c->attn_blocks_per_sm * kWarps;
-  plan_kernel<<<1, kPlanThreads, size_t(2) * p.Bt * sizeof(int32_t), st>>>(pp, p.MBF * p.B);
+  plan_kernel<<<1, kPlanThreads, size_t(2) * p.Bt * sizeof(int32_t), st>>>(pp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   attn_kernel<<<c->sms * c->attn_blocks_per_sm, kWarps * 32, kAttnSmem, st>>>(p);
