@@ -90,76 +90,23 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__
 }
 
 // =========================================================================
-// Planner (one CTA of 1024 threads)
+// Planner (one CTA)
 // =========================================================================
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 256;
+constexpr int kPlanWarps = kPlanThreads / 32;
 constexpr int kUnitsPerWarp = 8;   // minimum work units per resident warp
-constexpr int kSortMax = 2048;
+constexpr int kSplitCands = 22;    // candidate split lengths kMinSplit << k
+constexpr int kRemBuckets = 256;   // remainder size classes for the largest-first order
 
-__device__ int64_t block_sum64(int64_t v, int64_t* red) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+__device__ __forceinline__ int warp_sum(int v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  __syncthreads();
-  if (lane == 0) red[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    int64_t x = lane < nw ? red[lane] : 0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
-    if (lane == 0) red[0] = x;
-  }
-  __syncthreads();
-  const int64_t r = red[0];
-  __syncthreads();
-  return r;
+  return v;
 }
-
-__device__ int block_max(int v, int* red) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+__device__ __forceinline__ long long warp_sum64(long long v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(kFull, v, o));
-  __syncthreads();
-  if (lane == 0) red[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    int x = lane < nw ? red[lane] : 0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x = max(x, __shfl_xor_sync(kFull, x, o));
-    if (lane == 0) red[0] = x;
-  }
-  __syncthreads();
-  const int r = red[0];
-  __syncthreads();
-  return r;
-}
-
-// Exclusive scan of one int per thread; *total gets the block sum.
-__device__ int block_excl_scan(int v, int* red, int* total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(kFull, x, o);
-    if (lane >= o) x += y;
-  }
-  __syncthreads();
-  if (lane == 31) red[w] = x;
-  __syncthreads();
-  if (w == 0) {
-    int s = lane < nw ? red[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(kFull, s, o);
-      if (lane >= o) s += y;
-    }
-    red[lane] = s;
-  }
-  __syncthreads();
-  const int base = w > 0 ? red[w - 1] : 0;
-  *total = red[nw - 1];
-  __syncthreads();
-  return base + x - v;
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
 }
 
 // Work entries are int4 descriptors: {row b, t_begin, t_end, w} with
@@ -169,16 +116,20 @@ __device__ int block_excl_scan(int v, int* red, int* total) {
 // first; then one sliding-window entry per active row; then zero-fill units
 // (one per inactive row and layer).
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams p) {
+  // let the attention grid launch now; it waits for this grid before reading the plan
+  asm volatile("griddepcontrol.launch_dependents;");
   extern __shared__ int32_t plan_sm[];
-  int32_t* Ls = plan_sm;        // clamped context length per row (0 = no work)
-  int32_t* rem = plan_sm + p.Bt;
-  __shared__ int64_t red64[32];
-  __shared__ int red[32];
-  const int tid = threadIdx.x;
-  const int chunk = (p.Bt + blockDim.x - 1) / blockDim.x;
+  int32_t* Ls = plan_sm;  // clamped context length per row (0 = no work)
+  __shared__ long long s_units[kSplitCands], s_need[kSplitCands];
+  __shared__ long long s_red[3][kPlanWarps];
+  __shared__ int s_bucket[kRemBuckets];
+  __shared__ int4 s_scan[kPlanWarps];
+  __shared__ int s_S_log;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int chunk = (p.Bt + kPlanThreads - 1) / kPlanThreads;
   const int b_lo = min(p.Bt, tid * chunk), b_hi = min(p.Bt, b_lo + chunk);
 
-  int64_t tsum = 0;
+  long long tsum = 0;
   int lmax = 0, nact = 0;
   for (int b = b_lo; b < b_hi; ++b) {
     int L = 0;
@@ -199,76 +150,137 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     tsum += L;
     lmax = max(lmax, L);
   }
-  const int64_t T = block_sum64(tsum, red64);
-  const int Lmax = block_max(lmax, red);
-  const int64_t NAct = block_sum64(nact, red64);
+  for (int k = tid; k < kRemBuckets; k += kPlanThreads) s_bucket[k] = 0;
+  tsum = warp_sum64(tsum);
+  nact = warp_sum(nact);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lmax = max(lmax, __shfl_xor_sync(kFull, lmax, o));
+  if (lane == 0) {
+    s_red[0][wid] = tsum;
+    s_red[1][wid] = lmax;
+    s_red[2][wid] = nact;
+  }
+  __syncthreads();
+  long long T = 0, NAct = 0;
+  int Lmax = 0;
+  for (int w = 0; w < kPlanWarps; ++w) {
+    T += s_red[0][w];
+    Lmax = max(Lmax, int(s_red[1][w]));
+    NAct += s_red[2][w];
+  }
+
+  // unit counts and split-record needs of every candidate split length,
+  // one candidate per warp at a time
+  for (int k = wid; k < kSplitCands; k += kPlanWarps) {
+    const long long S = (long long)kMinSplit << k;
+    long long units = 0, need = 0;
+    for (int b = lane; b < p.Bt; b += 32) {
+      const int L = Ls[b];
+      if (L > 0) {
+        const long long c = (L + S - 1) / S;
+        units += c;
+        if (L > S) need += c;
+      }
+    }
+    units = warp_sum64(units);
+    need = warp_sum64(need);
+    if (lane == 0) {
+      s_units[k] = units;
+      s_need[k] = need;
+    }
+  }
+  __syncthreads();
   const int planes = (p.NL >> 1) * p.Hkv;
-  const int64_t warps = max(1, p.n_warps);
-
-  // Split length S (a power of two >= kMinSplit).  Start near a quarter of
-  // one warp's share of the full-layer work, then halve while there are
-  // fewer than kUnitsPerWarp units per resident warp (uniform long rows need
-  // many chunks; mixed rows balance through largest-first order).  Then cap
-  // the chunks per row and fit the partial records into the workspace.
-  int64_t S = kMinSplit;
-  const int64_t share = (T * planes) / (warps * 4);
-  while (S < share && S < (int64_t(1) << 30)) S <<= 1;
-  while (S > kMinSplit) {
-    int64_t units = 0;
-    for (int b = b_lo; b < b_hi; ++b)
-      if (Ls[b] > 0) units += (Ls[b] + S - 1) / S;
-    units = (block_sum64(units, red64) + NAct) * planes;
-    if (units >= kUnitsPerWarp * warps) break;
-    S >>= 1;
+  const long long warps = max(1, p.n_warps);
+  if (tid == 0) {
+    // Split length S = kMinSplit << k.  Start near a quarter of one warp's
+    // share of the full-layer work, then halve while there are fewer than
+    // kUnitsPerWarp units per resident warp (uniform long rows need many
+    // chunks; mixed rows balance through largest-first order).  Then cap the
+    // chunks per row and fit the partial records into the workspace.
+    const long long share = (T * planes) / (warps * 4);
+    int k = 0;
+    while (k < kSplitCands - 1 && ((long long)kMinSplit << k) < share) ++k;
+    while (k > 0 && (s_units[k] + NAct) * planes < kUnitsPerWarp * warps) --k;
+    while (k < kSplitCands - 1 && ((long long)kMinSplit << k) * kMaxSplitsPerRow < Lmax) ++k;
+    while (k < kSplitCands - 1 && s_need[k] > p.cap) ++k;
+    s_S_log = k;
   }
-  while (S * kMaxSplitsPerRow < Lmax) S <<= 1;
-  for (;;) {
-    int64_t need = 0;
-    for (int b = b_lo; b < b_hi; ++b)
-      if (Ls[b] > S) need += (Ls[b] + S - 1) / S;
-    need = block_sum64(need, red64);
-    if (need <= p.cap || S >= (int64_t(1) << 30)) break;
-    S <<= 1;
-  }
+  __syncthreads();
+  const int S_log = s_S_log;
+  const long long S = (long long)kMinSplit << S_log;
+  const int bshift = max(0, S_log + 9 - 8);  // remainder -> one of 256 classes
 
-  int n_full = 0, n_rem = 0, n_split = 0, n_act = 0, n_inact = 0;
+  // per-thread counts -> one packed exclusive scan: (full chunks, split
+  // records, active rows, remainders)
+  int4 cnt = make_int4(0, 0, 0, 0);
   for (int b = b_lo; b < b_hi; ++b) {
     const int L = Ls[b];
     if (L > 0) {
       const int nf = int(L / S), r = int(L % S), ns = nf + (r > 0);
-      rem[b] = r;
-      n_full += nf;
-      n_rem += (r > 0);
-      n_split += ns > 1 ? ns : 0;
-      ++n_act;
-    } else {
-      rem[b] = 0;
-      ++n_inact;
+      cnt.x += nf;
+      cnt.y += ns > 1 ? ns : 0;
+      cnt.z += 1;
+      if (r > 0) {
+        cnt.w += 1;
+        atomicAdd(&s_bucket[kRemBuckets - 1 - (r >> bshift)], 1);  // largest first
+      }
     }
   }
-  int A, R, TS, NA, NI;
-  int fp = block_excl_scan(n_full, red, &A);       // also syncs rem[] writes
-  int rp = block_excl_scan(n_rem, red, &R);
-  int sp = block_excl_scan(n_split, red, &TS);
-  int ap = block_excl_scan(n_act, red, &NA);
-  int ip = block_excl_scan(n_inact, red, &NI);
+  int4 inc = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(kFull, inc.x, o), y = __shfl_up_sync(kFull, inc.y, o);
+    const int z = __shfl_up_sync(kFull, inc.z, o), w = __shfl_up_sync(kFull, inc.w, o);
+    if (lane >= o) {
+      inc.x += x;
+      inc.y += y;
+      inc.z += z;
+      inc.w += w;
+    }
+  }
+  if (lane == 31) s_scan[wid] = inc;
+  __syncthreads();
+  int4 base = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
+  for (int w = 0; w < kPlanWarps; ++w) {
+    const int4 v = s_scan[w];
+    if (w < wid) {
+      base.x += v.x;
+      base.y += v.y;
+      base.z += v.z;
+      base.w += v.w;
+    }
+    tot.x += v.x;
+    tot.y += v.y;
+    tot.z += v.z;
+    tot.w += v.w;
+  }
+  if (tid == 0) {  // bucket counts -> exclusive offsets (one thread; 256 entries)
+    int acc = 0;
+    for (int k = 0; k < kRemBuckets; ++k) {
+      const int c = s_bucket[k];
+      s_bucket[k] = acc;
+      acc += c;
+    }
+  }
+  __syncthreads();
+  int fp = base.x + inc.x - cnt.x;
+  int sp = base.y + inc.y - cnt.y;
+  int ap = base.z + inc.z - cnt.z;
+  const int A = tot.x, TS = tot.y, NA = tot.z, R = tot.w;
   const int NEF = A + R;  // full-layer entries
+  int ip = b_lo - ap;     // inactive rows before this thread's rows
+  (void)R;
 
   for (int b = b_lo; b < b_hi; ++b) {
     const int L = Ls[b];
     if (L > 0) {
-      const int nf = int(L / S), r = rem[b], ns = nf + (r > 0);
+      const int nf = int(L / S), r = int(L % S), ns = nf + (r > 0);
       for (int s = 0; s < nf; ++s)
         p.edesc[fp++] = make_int4(b, int(s * S), int((s + 1) * S), s | (ns << 16));
       if (r > 0) {
-        int rank;
-        if (p.Bt <= kSortMax) {  // remainders largest first, ties by row
-          rank = 0;
-          for (int c = 0; c < p.Bt; ++c) rank += (rem[c] > r) || (rem[c] == r && c < b);
-        } else {
-          rank = rp++;
-        }
-        p.edesc[A + rank] = make_int4(b, int(nf * S), L, nf | (ns << 16));
+        const int slot = atomicAdd(&s_bucket[kRemBuckets - 1 - (r >> bshift)], 1);
+        p.edesc[A + slot] = make_int4(b, int(nf * S), L, nf | (ns << 16));
       }
       if (ns > 1) {
         p.part_base[b] = sp;
@@ -294,7 +306,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     if (TS > p.cap) set_error(GK_DEVERR_PLAN);
     p.hdr[kHdrQueue] = 0;
     p.hdr[kHdrNUnits] = (NEF + NA) * planes;
-    p.hdr[kHdrNZero] = NI * p.NL;
+    p.hdr[kHdrNZero] = (p.Bt - NA) * p.NL;
     p.hdr[kHdrSplit] = int(S);
     p.hdr[kHdrNEntries] = NEF + NA;
     p.hdr[kHdrTotalSplits] = TS;
@@ -384,6 +396,8 @@ __global__ void __launch_bounds__(kWarps * 32, 4) attn_kernel(const __grid_const
   }
   __syncwarp();
 
+  // the planner grid (launched just before) must be complete from here on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int nU = p.hdr[kHdrNUnits], nZ = p.hdr[kHdrNZero];
   const int planes = (p.NL >> 1) * p.Hkv;
 
@@ -898,7 +912,7 @@ static cudaError_t device_setup(DeviceCache** out) {
                              int(kAttnSmem));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(2 * kMaxBatch * sizeof(int32_t)));
+                             int(kMaxBatch * sizeof(int32_t)));
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.attn_blocks_per_sm, attn_kernel,
                                                       kWarps * 32, kAttnSmem);
@@ -945,11 +959,22 @@ cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaSt
   if (e != cudaSuccess) return e;
   PlanParams pp = plan;
   pp.n_warps = c->sms * c->attn_blocks_per_sm * kWarps;
-  plan_kernel<<<1, kPlanThreads, size_t(2) * p.Bt * sizeof(int32_t), st>>>(pp);
+  plan_kernel<<<1, kPlanThreads, size_t(p.Bt) * sizeof(int32_t), st>>>(pp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_kernel<<<c->sms * c->attn_blocks_per_sm, kWarps * 32, kAttnSmem, st>>>(p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the attention CTAs start while the
+  // planner runs and wait for it (griddepcontrol.wait) before reading its plan
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(c->sms * c->attn_blocks_per_sm));
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = kAttnSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_kernel, p);
 }
 
 cudaError_t read_device_error(cudaStream_t st, uint32_t* bits, bool clear) {
