@@ -207,6 +207,82 @@ def oracle_sample(w, c, step_host, cache, budget_s: float, seed: int = 0, rows_m
     return done / spent, done, spent, used
 
 
+# ------------------------------------------------------------------ end-to-end loop
+def run_e2e(gk, shape, inputs, kb, vb, out, ws, stream, dev, K, W, units, dist):
+    """Time K steps fed from pinned host memory: per step one H2D copy of all
+    inputs (packed), append + attention, one D2H copy of the output.  Returns
+    (max ms over ranks, units over ranks, H2D bytes/step, D2H bytes/step)."""
+    import torch
+    names = list(inputs)
+    offs, off = {}, 0
+    for n in names:
+        nb = inputs[n].numel() * inputs[n].element_size()
+        offs[n] = off
+        off += (nb + 255) // 256 * 256
+    total = off
+    host = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for n in names:
+        t = inputs[n]
+        nb = t.numel() * t.element_size()
+        host[offs[n]:offs[n] + nb].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+    dbuf = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+
+    def views(buf):
+        v = {}
+        for n in names:
+            t = inputs[n]
+            nb = t.numel() * t.element_size()
+            v[n] = buf[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
+        return v
+
+    dv = [views(b) for b in dbuf]
+    outs = [out, torch.empty_like(out)]
+    host_out = torch.empty(out.numel() * out.element_size(), dtype=torch.uint8).pin_memory()
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    sh = stream.cuda_stream
+
+    def step(k):
+        i = k % 2
+        d = dv[i]
+        if k >= 2:
+            s_in.wait_event(ev_done[i])          # kernels of step k-2 are done with buffer i
+        with torch.cuda.stream(s_in):
+            dbuf[i].copy_(host, non_blocking=True)
+            ev_in[i].record(s_in)
+        stream.wait_event(ev_in[i])
+        if k >= 2:
+            stream.wait_event(ev_out[i])         # output i of step k-2 has been read back
+        gk.gk_kv_append(shape, d["k_new"], d["v_new"], d["cos"], d["sin"], d["k_scale"],
+                        d["v_scale"], d["upd_full"], d["upd_swa"], d["active"], kb, vb, stream=sh)
+        gk.gk_decode_attn_stack(shape, d["q"], kb, vb, d["k_scale"], d["v_scale"], d["cos"],
+                                d["sin"], d["bt_full"], d["bt_swa"], d["pos"], d["pos_w"],
+                                d["active"], outs[i], None, ws, stream=sh)
+        ev_done[i].record(stream)
+        s_out.wait_event(ev_done[i])
+        with torch.cuda.stream(s_out):
+            host_out.copy_(outs[i].view(-1).view(torch.uint8), non_blocking=True)
+            ev_out[i].record(s_out)
+
+    for k in range(W):
+        step(k)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for k in range(K):
+        step(k)
+    e1.record(s_out)
+    torch.cuda.synchronize(dev)
+    ms, u = reduce_timing(e0.elapsed_time(e1), units * K, dist, dev)
+    return ms, u, total, host_out.numel()
+
+
 # ------------------------------------------------------------------ main arms
 def run_gk(args):
     import torch
@@ -282,39 +358,12 @@ def run_gk(args):
     value = total_units / (max_ms / 1e3)
     ms_per_step = max_ms / K
 
-    # ---- end to end: inputs from pinned host memory, output back to host
-    host_in = {k: v.cpu().pin_memory() for k, v in
-               dict(q=q, k_new=k_new, v_new=v_new, **ctl).items()}
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = host_out.numel() * host_out.element_size()
-
-    def e2e_step():
-        for k_, v_ in host_in.items():
-            dev_in[k_].copy_(v_, non_blocking=True)
-        gk.gk_kv_append(shape, dev_in["k_new"], dev_in["v_new"], dev_in["cos"], dev_in["sin"],
-                        dev_in["k_scale"], dev_in["v_scale"], dev_in["upd_full"],
-                        dev_in["upd_swa"], dev_in["active"], kb, vb, stream=sh)
-        gk.gk_decode_attn_stack(shape, dev_in["q"], kb, vb, dev_in["k_scale"], dev_in["v_scale"],
-                                dev_in["cos"], dev_in["sin"], dev_in["bt_full"], dev_in["bt_swa"],
-                                dev_in["pos"], dev_in["pos_w"], dev_in["active"], out, None, ws,
-                                stream=sh)
-        host_out.copy_(out, non_blocking=True)
-
-    for _ in range(W):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    if dist:
-        dist.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(K):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms, e2e_units = reduce_timing(e0.elapsed_time(e1), units * K, dist, dev)
+    # ---- end to end: every step's inputs copied from pinned host memory (one
+    # packed staging copy) and its output copied back, double-buffered on two
+    # copy streams so that step k+1's upload and step k's download overlap
+    # step k's kernels.
+    e2e_ms, e2e_units, h2d, d2h = run_e2e(gk, shape, dict(q=q, k_new=k_new, v_new=v_new, **ctl),
+                                          kb, vb, out, ws, stream, dev, K, W, units, dist)
     if gk.gk_read_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
 
