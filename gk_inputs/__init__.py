@@ -123,6 +123,8 @@ REDUCED = {
 # 0.7 GB of KV per step (larger than L2, small enough for a full counter set).
 PROFILE = {
     "gptoss_b8": WORKLOADS["gptoss_b64"].replace(name="gptoss_b8", batch=8, seed=22),
+    "gptoss_b16": WORKLOADS["gptoss_b64"].replace(name="gptoss_b16", batch=16, seed=23),
+    "swa_b128": WORKLOADS["swa_b512"].replace(name="swa_b128", batch=128, seed=24),
 }
 
 

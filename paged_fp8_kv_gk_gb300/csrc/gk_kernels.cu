@@ -26,65 +26,102 @@ __device__ uint32_t g_dev_error;
 
 __device__ __forceinline__ void set_error(uint32_t bits) { atomicOr(&g_dev_error, bits); }
 
+// 1/s when s is a power of two whose reciprocal is a normal float (then
+// x * (1/s) is exactly the correctly rounded x / s for every x); 0 otherwise.
+__device__ __forceinline__ float exact_reciprocal(float s) {
+  const uint32_t u = __float_as_uint(s);
+  const uint32_t e = (u >> 23) & 0xffu;
+  if ((u & 0x7fffffu) != 0 || e < 2 || e > 252) return 0.f;
+  return __uint_as_float((u & 0x80000000u) | ((254u - e) << 23));
+}
+
+// x / s with IEEE round-to-nearest; r = exact_reciprocal(s) when nonzero.
+__device__ __forceinline__ float div_scale(float x, float s, float r) {
+  return r != 0.f ? x * r : __fdiv_rn(x, s);
+}
+
 // =========================================================================
 // KV append
 // =========================================================================
-// One warp per (layer i, row b, kv head h).  Lane l rotates the pair
-// (l, l + 32) of k and converts channels 2l, 2l + 1 of v.
+// One warp per (layer i, row b); kv heads in groups of 8.  Lane l rotates
+// the pair (l, l + 32) of k and converts channels 2l, 2l + 1 of v.  All of a
+// group's loads are issued before any of them is used (one memory round trip
+// per group rather than a chain of dependent ones).
+constexpr int kAppendHeads = 8;
+
 __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ AppendParams p) {
+  // The decode-attention planner may launch now: it reads only positions and
+  // the active mask, and waits for this grid before it exits.
+  asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t total = int64_t(p.NL) * p.Bt * p.Hkv;
-  if (row >= total) return;
-  const int h = int(row % p.Hkv);
-  const int64_t ib = row / p.Hkv;
+  const int64_t ib = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (ib >= int64_t(p.NL) * p.Bt) return;
   const int b = int(ib % p.Bt);
   const int i = int(ib / p.Bt);
-  if (!p.active[b]) return;
+  const uint16_t* kr = p.k_new + ib * p.Hkv * kHeadDim;
+  const uint32_t* vr = reinterpret_cast<const uint32_t*>(p.v_new + ib * p.Hkv * kHeadDim);
   // layer parity: even = sliding window (upd_swa), odd = full (upd_full)
+  const uint8_t act = p.active[b];
   const int32_t slot = (i & 1) ? p.upd_full[b] : p.upd_swa[b];
-  if (slot < 0 || int64_t(slot) >= int64_t(p.nb) * p.B) {
-    if (lane == 0) set_error(GK_DEVERR_SLOT);
-    return;
-  }
-  const int64_t pb = slot / p.B;
-  const int t = slot % p.B;
-  const uint16_t* kr = p.k_new + row * kHeadDim;
-  const uint16_t* vr = p.v_new + row * kHeadDim;
-
-  const float x = __uint_as_float(uint32_t(kr[lane]) << 16);
-  const float y = __uint_as_float(uint32_t(kr[lane + 32]) << 16);
   const float c = p.cosb[b * (kHeadDim / 2) + lane];
   const float s = p.sinb[b * (kHeadDim / 2) + lane];
-  // fixed fp32 sequence, every operation rounded on its own (no contraction)
-  const float xr = __fsub_rn(__fmul_rn(x, c), __fmul_rn(y, s));
-  const float yr = __fadd_rn(__fmul_rn(y, c), __fmul_rn(x, s));
   const float ks = p.k_scale[i];
-  const uint32_t kc = f32x2_to_e4m3x2(__fdiv_rn(xr, ks), __fdiv_rn(yr, ks));
-  // packed K: tokens 2p and 2p+1 interleaved per channel
-  uint8_t* kdst =
-      p.kb[i >> 1] + ((pb * p.Hkv + h) * (p.B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1);
-  kdst[2 * lane] = uint8_t(kc & 0xffu);
-  kdst[2 * (lane + 32)] = uint8_t(kc >> 8);
-
-  const uint32_t vw = reinterpret_cast<const uint32_t*>(vr)[lane];
   const float vs = p.v_scale[i];
-  const uint32_t vc =
-      f32x2_to_e4m3x2(__fdiv_rn(bf16lo_to_f32(vw), vs), __fdiv_rn(bf16hi_to_f32(vw), vs));
-  uint8_t* vdst = p.vb[i >> 1] + ((pb * p.Hkv + h) * p.B + t) * kHeadDim;
-  reinterpret_cast<uint16_t*>(vdst)[lane] = uint16_t(vc);
+  for (int h0 = 0; h0 < p.Hkv; h0 += kAppendHeads) {
+    const int nh = min(kAppendHeads, p.Hkv - h0);
+    uint32_t kx[kAppendHeads], ky[kAppendHeads], vw[kAppendHeads];
+#pragma unroll
+    for (int k = 0; k < kAppendHeads; ++k) {
+      if (k < nh) {
+        kx[k] = kr[(h0 + k) * kHeadDim + lane];
+        ky[k] = kr[(h0 + k) * kHeadDim + lane + 32];
+        vw[k] = vr[(h0 + k) * (kHeadDim / 2) + lane];
+      }
+    }
+    if (!act) return;
+    if (slot < 0 || int64_t(slot) >= int64_t(p.nb) * p.B) {
+      if (lane == 0) set_error(GK_DEVERR_SLOT);
+      return;
+    }
+    const int64_t pb = slot / p.B;
+    const int t = slot % p.B;
+    const float kr_inv = exact_reciprocal(ks), vr_inv = exact_reciprocal(vs);
+    // packed K: tokens 2p and 2p+1 interleaved per channel; head h is (B/2) pair rows further
+    uint8_t* kdst =
+        p.kb[i >> 1] + ((pb * p.Hkv + h0) * (p.B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1);
+    uint8_t* vdst = p.vb[i >> 1] + ((pb * p.Hkv + h0) * p.B + t) * kHeadDim;
+    const int64_t kstride = int64_t(p.B >> 1) * (2 * kHeadDim), vstride = int64_t(p.B) * kHeadDim;
+#pragma unroll
+    for (int k = 0; k < kAppendHeads; ++k) {
+      if (k < nh) {
+        const float x = __uint_as_float(kx[k] << 16);
+        const float y = __uint_as_float(ky[k] << 16);
+        // fixed fp32 sequence, every operation rounded on its own (no contraction)
+        const float xr = __fsub_rn(__fmul_rn(x, c), __fmul_rn(y, s));
+        const float yr = __fadd_rn(__fmul_rn(y, c), __fmul_rn(x, s));
+        const uint32_t kc =
+            f32x2_to_e4m3x2(div_scale(xr, ks, kr_inv), div_scale(yr, ks, kr_inv));
+        kdst[k * kstride + 2 * lane] = uint8_t(kc & 0xffu);
+        kdst[k * kstride + 2 * (lane + 32)] = uint8_t(kc >> 8);
+        const uint32_t vc = f32x2_to_e4m3x2(div_scale(bf16lo_to_f32(vw[k]), vs, vr_inv),
+                                            div_scale(bf16hi_to_f32(vw[k]), vs, vr_inv));
+        reinterpret_cast<uint16_t*>(vdst + k * vstride)[lane] = uint16_t(vc);
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ x, float scale,
                                                        uint8_t* __restrict__ codes, int64_t n) {
   const int64_t stride = int64_t(gridDim.x) * blockDim.x * 2;
+  const float r = exact_reciprocal(scale);
   for (int64_t i = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 2; i < n; i += stride) {
     if (i + 1 < n) {
-      const uint32_t c = f32x2_to_e4m3x2(__fdiv_rn(x[i], scale), __fdiv_rn(x[i + 1], scale));
+      const uint32_t c = f32x2_to_e4m3x2(div_scale(x[i], scale, r), div_scale(x[i + 1], scale, r));
       codes[i] = uint8_t(c & 0xffu);
       codes[i + 1] = uint8_t(c >> 8);
     } else {
-      codes[i] = uint8_t(f32x2_to_e4m3x2(__fdiv_rn(x[i], scale), 0.f) & 0xffu);
+      codes[i] = uint8_t(f32x2_to_e4m3x2(div_scale(x[i], scale, r), 0.f) & 0xffu);
     }
   }
 }
@@ -255,12 +292,25 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     tot.z += v.z;
     tot.w += v.w;
   }
-  if (tid == 0) {  // bucket counts -> exclusive offsets (one thread; 256 entries)
-    int acc = 0;
-    for (int k = 0; k < kRemBuckets; ++k) {
-      const int c = s_bucket[k];
-      s_bucket[k] = acc;
-      acc += c;
+  if (wid == 0) {  // bucket counts -> exclusive offsets: 8 buckets per lane, one warp scan
+    constexpr int per = kRemBuckets / 32;
+    int v[per], sum = 0;
+#pragma unroll
+    for (int k = 0; k < per; ++k) {
+      v[k] = s_bucket[lane * per + k];
+      sum += v[k];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int acc = incl - sum;
+#pragma unroll
+    for (int k = 0; k < per; ++k) {
+      s_bucket[lane * per + k] = acc;
+      acc += v[k];
     }
   }
   __syncthreads();
@@ -311,6 +361,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     p.hdr[kHdrNEntries] = NEF + NA;
     p.hdr[kHdrTotalSplits] = TS;
   }
+  // This grid may have started while the kernel before it (the KV append)
+  // was still running; it completes only after that kernel has, so the
+  // attention grid that waits on this one also sees the appended KV.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // =========================================================================
@@ -932,7 +986,7 @@ int attention_resident_warps() {
 }
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t st) {
-  const int64_t warps = int64_t(p.NL) * p.Bt * p.Hkv;
+  const int64_t warps = int64_t(p.NL) * p.Bt;
   if (warps == 0) return cudaSuccess;
   const int threads = 256;
   const int64_t blocks = (warps * 32 + threads - 1) / threads;
@@ -959,19 +1013,27 @@ cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaSt
   if (e != cudaSuccess) return e;
   PlanParams pp = plan;
   pp.n_warps = c->sms * c->attn_blocks_per_sm * kWarps;
-  plan_kernel<<<1, kPlanThreads, size_t(p.Bt) * sizeof(int32_t), st>>>(pp);
-  e = cudaGetLastError();
+  // Programmatic dependent launches: the planner may overlap the kernel before
+  // it (it reads no KV and waits for that kernel before exiting); the
+  // attention CTAs start while the planner runs and wait for it
+  // (griddepcontrol.wait) before reading its plan.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t pcfg = {};
+  pcfg.gridDim = dim3(1);
+  pcfg.blockDim = dim3(kPlanThreads);
+  pcfg.dynamicSmemBytes = size_t(p.Bt) * sizeof(int32_t);
+  pcfg.stream = st;
+  pcfg.attrs = attr;
+  pcfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&pcfg, plan_kernel, pp);
   if (e != cudaSuccess) return e;
-  // programmatic dependent launch: the attention CTAs start while the
-  // planner runs and wait for it (griddepcontrol.wait) before reading its plan
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(c->sms * c->attn_blocks_per_sm));
   cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = kAttnSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, attn_kernel, p);
