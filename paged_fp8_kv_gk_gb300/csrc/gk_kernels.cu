@@ -156,7 +156,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   // let the attention grid launch now; it waits for this grid before reading the plan
   asm volatile("griddepcontrol.launch_dependents;");
   extern __shared__ int32_t plan_sm[];
-  int32_t* Ls = plan_sm;  // clamped context length per row (0 = no work)
+  int32_t* Ls = plan_sm;          // clamped context length per row (0 = no work)
+  int32_t* Pw = plan_sm + p.Bt;   // window-frame position per row
   __shared__ long long s_units[kSplitCands], s_need[kSplitCands];
   __shared__ long long s_red[3][kPlanWarps];
   __shared__ int s_bucket[kRemBuckets];
@@ -170,8 +171,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   int lmax = 0, nact = 0;
   for (int b = b_lo; b < b_hi; ++b) {
     int L = 0;
-    if (p.active[b]) {
-      const int pos = p.pos[b];
+    const int act = p.active[b], pos = p.pos[b];   // one round trip for all three
+    Pw[b] = p.pos_w[b];
+    if (act) {
       if (pos < 0) {
         set_error(GK_DEVERR_POS);
       } else {
@@ -209,12 +211,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   // unit counts and split-record needs of every candidate split length,
   // one candidate per warp at a time
   for (int k = wid; k < kSplitCands; k += kPlanWarps) {
-    const long long S = (long long)kMinSplit << k;
+    const int sh = 9 + k;  // log2 of kMinSplit << k
+    const long long S = 1ll << sh;
     long long units = 0, need = 0;
     for (int b = lane; b < p.Bt; b += 32) {
       const int L = Ls[b];
       if (L > 0) {
-        const long long c = (L + S - 1) / S;
+        const long long c = (L + S - 1) >> sh;
         units += c;
         if (L > S) need += c;
       }
@@ -245,7 +248,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   }
   __syncthreads();
   const int S_log = s_S_log;
-  const long long S = (long long)kMinSplit << S_log;
+  const int S_sh = 9 + S_log;  // S = 2^S_sh
+  const long long S = 1ll << S_sh;
+  static_assert(kMinSplit == 512, "split lengths are 2^(9 + k)");
   const int bshift = max(0, S_log + 9 - 8);  // remainder -> one of 256 classes
 
   // per-thread counts -> one packed exclusive scan: (full chunks, split
@@ -254,7 +259,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   for (int b = b_lo; b < b_hi; ++b) {
     const int L = Ls[b];
     if (L > 0) {
-      const int nf = int(L / S), r = int(L % S), ns = nf + (r > 0);
+      const int nf = int(L >> S_sh), r = int(L & (S - 1)), ns = nf + (r > 0);
       cnt.x += nf;
       cnt.y += ns > 1 ? ns : 0;
       cnt.z += 1;
@@ -325,7 +330,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   for (int b = b_lo; b < b_hi; ++b) {
     const int L = Ls[b];
     if (L > 0) {
-      const int nf = int(L / S), r = int(L % S), ns = nf + (r > 0);
+      const int nf = int(L >> S_sh), r = int(L & (S - 1)), ns = nf + (r > 0);
       for (int s = 0; s < nf; ++s)
         p.edesc[fp++] = make_int4(b, int(s * S), int((s + 1) * S), s | (ns << 16));
       if (r > 0) {
@@ -341,7 +346,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         p.part_base[b] = 0;
       }
       // sliding-window layer of this row: keys [max(0, pos_w - W + 1), pos_w]
-      int pw = p.pos_w[b];
+      int pw = Pw[b];
       if (pw < 0 || pw >= p.max_tokens_swa) {
         set_error(GK_DEVERR_POS);
         pw = min(max(pw, 0), p.max_tokens_swa - 1);
@@ -966,7 +971,7 @@ static cudaError_t device_setup(DeviceCache** out) {
                              int(kAttnSmem));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kMaxBatch * sizeof(int32_t)));
+                             int(2 * kMaxBatch * sizeof(int32_t)));
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.attn_blocks_per_sm, attn_kernel,
                                                       kWarps * 32, kAttnSmem);
@@ -1023,7 +1028,7 @@ cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaSt
   cudaLaunchConfig_t pcfg = {};
   pcfg.gridDim = dim3(1);
   pcfg.blockDim = dim3(kPlanThreads);
-  pcfg.dynamicSmemBytes = size_t(p.Bt) * sizeof(int32_t);
+  pcfg.dynamicSmemBytes = size_t(2) * p.Bt * sizeof(int32_t);
   pcfg.stream = st;
   pcfg.attrs = attr;
   pcfg.numAttrs = 1;
