@@ -16,6 +16,8 @@
 // contract" (layer parity i % 2 selects table / index / position, buffer
 // i / 2) and "KV-cache layout" (packed K view [.., block/2, d, 2], plain V).
 #include <cuda_runtime.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "gk_device.cuh"
 #include "gk_internal.h"
@@ -395,19 +397,29 @@ constexpr uint32_t kQBytes = kGroup * kHeadDim * 2;
 constexpr uint32_t kRopeBytes = (kHeadDim / 2) * 4;
 constexpr uint32_t kUnitHeadBytes = kQBytes + 2 * kRopeBytes;
 
+// The FMA comparison path keeps q' in fp32 (rows padded so the eight heads
+// fall in different banks) and one stage of P for the exchange between its
+// token-per-lane and channel-per-lane phases.
+constexpr int kQfStride = kHeadDim + 4;
+
 // One per warp, laid out back to back: the 128-byte alignment keeps every
 // warp's ring and q buffer on the 16-byte boundary bulk copies require.
-struct alignas(128) WarpSmem {
+template <bool kMma>
+struct alignas(128) WarpSmemT {
   uint8_t ring[kStages][kStageBytes];
   uint8_t qbuf[kUnitHeadBytes];
+  float qf[kMma ? 4 : kGroup * kQfStride];
+  float pbuf[kMma ? 4 : kStageTok * kGroup];
   unsigned long long bar[kStages];
   UnitDesc fifo[kFifo];
 };
-static_assert(sizeof(WarpSmem) % 128 == 0, "warp areas must stay 128-byte aligned");
+static_assert(sizeof(WarpSmemT<true>) % 128 == 0 && sizeof(WarpSmemT<false>) % 128 == 0,
+              "warp areas must stay 128-byte aligned");
 static_assert(kStageBytes % 16 == 0 && kUnitHeadBytes % 16 == 0 && kStageKBytes % 16 == 0,
               "bulk-copy destinations must be 16-byte aligned");
 
-constexpr size_t kAttnSmem = sizeof(WarpSmem) * kWarps;
+template <bool kMma>
+constexpr size_t attn_smem() { return sizeof(WarpSmemT<kMma>) * kWarps; }
 
 __device__ __forceinline__ void zero_row(const AttnParams& p, int layer, int b, int lane) {
   const int64_t base = (int64_t(layer) * p.Bt + b) * p.Hq * kHeadDim;
@@ -438,13 +450,18 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int u, int4 e, 
   d.n_st = (e.z + kStageTok - 1) / kStageTok - d.st_begin;
 }
 
+// kMma = true: QK^T and PV on the tensor cores (the product path).
+// kMma = false: the same pipeline with both products as fp32 FMA, kept to
+// measure the choice (selected with GK_ATTN_PATH=fma).
 // 4 CTAs (16 warps) per SM: latency hiding across warps measured worth more
 // than a deeper ring or the registers above 128.
-__global__ void __launch_bounds__(kWarps * 32, 4) attn_kernel(const __grid_constant__ AttnParams p) {
+template <bool kMma>
+__global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
+    attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, qd = lane & 3;
-  WarpSmem& ws = reinterpret_cast<WarpSmem*>(smem_raw)[warp];
+  WarpSmemT<kMma>& ws = reinterpret_cast<WarpSmemT<kMma>*>(smem_raw)[warp];
   const uint32_t ring0 = smem_u32(&ws.ring[0][0]);
   const uint32_t qbuf0 = smem_u32(&ws.qbuf[0]);
   const uint32_t bar0 = smem_u32(&ws.bar[0]);
@@ -635,6 +652,9 @@ __global__ void __launch_bounds__(kWarps * 32, 4) attn_kernel(const __grid_const
         thr1 = 0.f, vscale = 0.f;
   float o[4][4];
   float lacc[4];  // softmax denominators from a ones-row MMA over the f16 P
+  // FMA path: per-head reference maxima / thresholds (log2 units, warp-uniform)
+  // and this lane's partial denominators (lane = token)
+  float mh[kMma ? 1 : kGroup], thh[kMma ? 1 : kGroup], lsum[kMma ? 1 : kGroup];
 
   while (prod - cons < kStages && issue_next()) {
   }
@@ -684,6 +704,22 @@ __global__ void __launch_bounds__(kWarps * 32, 4) attn_kernel(const __grid_const
         r[2 * w + 1] = (bf16hi_to_f32(xw[w]) * c1 + sgn * bf16hi_to_f32(yw[w]) * s1) * ck;
         amax = fmaxf(amax, fmaxf(fabsf(r[2 * w]), fabsf(r[2 * w + 1])));
       }
+      if constexpr (!kMma) {
+        // q' (log2 units) in fp32 to shared memory: head g, channels 16qd..16qd+15
+        float* qrow_f = ws.qf + g * kQfStride + 16 * qd;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          reinterpret_cast<float4*>(qrow_f)[k] =
+              make_float4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) {
+          mh[h] = -INFINITY;
+          thh[h] = -INFINITY;
+          lsum[h] = 0.f;
+        }
+        si0 = si1 = 1.f;
+      }
       amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
       amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
       // power-of-two normalisation of the head so that max |q'| < 2^14 in f16
@@ -698,8 +734,10 @@ __global__ void __launch_bounds__(kWarps * 32, 4) attn_kernel(const __grid_const
         const float2 h = f16x2_to_f32x2(qhi[w]);
         qlo[w] = f32x2_to_f16x2(a - h.x, b - h.y);  // residual is exact in fp32
       }
-      si0 = __shfl_sync(kFull, finv, 8 * qd);   // heads 2qd and 2qd+1
-      si1 = __shfl_sync(kFull, finv, 8 * qd + 4);
+      if constexpr (kMma) {
+        si0 = __shfl_sync(kFull, finv, 8 * qd);   // heads 2qd and 2qd+1
+        si1 = __shfl_sync(kFull, finv, 8 * qd + 4);
+      }
       vscale = p.v_scale[cd.layer];
       mr0 = mr1 = thr0 = thr1 = -INFINITY;
       nb0 = nb1 = 0.f;
@@ -713,6 +751,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4) attn_kernel(const __grid_const
     const int tok0 = (cd.st_begin + k_in_unit) * kStageTok;
     const bool edge = tok0 < cd.t_begin || tok0 + kStageTok > cd.t_end;
 
+    if constexpr (kMma) {
     // ---- S = q' K^T for two 16-token tiles; rows (g, g+8) = tokens (2p, 2p+1)
     float sc[2][4];
 #pragma unroll
@@ -808,6 +847,101 @@ __global__ void __launch_bounds__(kWarps * 32, 4) attn_kernel(const __grid_const
         mma_f16(o[m], a0, a1, a2, a3, b0, b1);
       }
     }
+    }
+    if constexpr (!kMma) {
+      // ---- S = q' K^T with fp32 FMA; lane = token t of the stage
+      const int t = lane;
+      const uint32_t krow = Ks + (t >> 1) * (2 * kHeadDim);
+      const uint32_t sel = (t & 1) ? 0x7531u : 0x6420u;  // this token's byte of each pair
+      float sf[kGroup];
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) sf[h] = 0.f;
+#pragma unroll 2
+      for (int c = 0; c < kHeadDim / 8; ++c) {  // 8 channels per step
+        const uint4 w = lds128(krow + 16 * c);
+        uint32_t h01, h23, h45, h67;
+        e4m3x4_to_f16x2x2(prmt(w.x, w.y, sel), h01, h23);
+        e4m3x4_to_f16x2x2(prmt(w.z, w.w, sel), h45, h67);
+        const float2 k01 = f16x2_to_f32x2(h01), k23 = f16x2_to_f32x2(h23);
+        const float2 k45 = f16x2_to_f32x2(h45), k67 = f16x2_to_f32x2(h67);
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) {
+          const float4 qa = reinterpret_cast<const float4*>(ws.qf + h * kQfStride + 8 * c)[0];
+          const float4 qb = reinterpret_cast<const float4*>(ws.qf + h * kQfStride + 8 * c)[1];
+          sf[h] = fmaf(qa.x, k01.x, sf[h]);
+          sf[h] = fmaf(qa.y, k01.y, sf[h]);
+          sf[h] = fmaf(qa.z, k23.x, sf[h]);
+          sf[h] = fmaf(qa.w, k23.y, sf[h]);
+          sf[h] = fmaf(qb.x, k45.x, sf[h]);
+          sf[h] = fmaf(qb.y, k45.y, sf[h]);
+          sf[h] = fmaf(qb.z, k67.x, sf[h]);
+          sf[h] = fmaf(qb.w, k67.y, sf[h]);
+        }
+      }
+      const bool valid = !(edge && (tok0 + t < cd.t_begin || tok0 + t >= cd.t_end));
+      bool over = false;
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) {
+        if (!valid) sf[h] = -INFINITY;
+        over |= sf[h] > thh[h];
+      }
+      if (__any_sync(kFull, over)) {
+        float al[kGroup];
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) {
+          float wm = sf[h];
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) wm = fmaxf(wm, __shfl_xor_sync(kFull, wm, off));
+          const float n = fmaxf(mh[h], wm);
+          al[h] = ex2(mh[h] - n);
+          mh[h] = n;
+          thh[h] = n + kLazyLog2;
+          lsum[h] *= al[h];
+        }
+        float a0 = 1.f, a1 = 1.f;
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) {
+          if (h == 2 * qd) a0 = al[h];
+          if (h == 2 * qd + 1) a1 = al[h];
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          o[m][0] *= a0;
+          o[m][2] *= a0;
+          o[m][1] *= a1;
+          o[m][3] *= a1;
+        }
+      }
+      float pf[kGroup];
+#pragma unroll
+      for (int h = 0; h < kGroup; ++h) {
+        pf[h] = ex2(sf[h] - mh[h]);
+        lsum[h] += pf[h];
+      }
+      float4* prow = reinterpret_cast<float4*>(ws.pbuf + t * kGroup);
+      prow[0] = make_float4(pf[0], pf[1], pf[2], pf[3]);
+      prow[1] = make_float4(pf[4], pf[5], pf[6], pf[7]);
+      __syncwarp();
+      // ---- O += P V with fp32 FMA; lane (g, qd): heads 2qd, 2qd+1, channels 8g..8g+7
+      for (int tt = 0; tt < kStageTok; ++tt) {
+        if (edge && (tok0 + tt < cd.t_begin || tok0 + tt >= cd.t_end)) continue;
+        const float2 pp = reinterpret_cast<const float2*>(ws.pbuf + tt * kGroup + 2 * qd)[0];
+        const uint2 vv = lds64(Vs + tt * kHeadDim + 8 * g);
+        uint32_t v01, v23, v45, v67;
+        e4m3x4_to_f16x2x2(vv.x, v01, v23);
+        e4m3x4_to_f16x2x2(vv.y, v45, v67);
+        const float2 f01 = f16x2_to_f32x2(v01), f23 = f16x2_to_f32x2(v23);
+        const float2 f45 = f16x2_to_f32x2(v45), f67 = f16x2_to_f32x2(v67);
+        const float vf[8] = {f01.x, f01.y, f23.x, f23.y, f45.x, f45.y, f67.x, f67.y};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          o[m][0] = fmaf(pp.x, vf[2 * m], o[m][0]);
+          o[m][2] = fmaf(pp.x, vf[2 * m + 1], o[m][2]);
+          o[m][1] = fmaf(pp.y, vf[2 * m], o[m][1]);
+          o[m][3] = fmaf(pp.y, vf[2 * m + 1], o[m][3]);
+        }
+      }
+    }
     __syncwarp();
     ++cons;
     ++k_in_unit;
@@ -818,6 +952,21 @@ __global__ void __launch_bounds__(kWarps * 32, 4) attn_kernel(const __grid_const
       // ---- unit epilogue
       k_in_unit = 0;
       ++f_head;
+      if constexpr (!kMma) {
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h) {
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) lsum[h] += __shfl_xor_sync(kFull, lsum[h], off);
+          if (h == 2 * qd) {
+            lacc[0] = lsum[h];
+            mr0 = mh[h];
+          }
+          if (h == 2 * qd + 1) {
+            lacc[1] = lsum[h];
+            mr1 = mh[h];
+          }
+        }
+      }
       const float l0 = lacc[0], l1 = lacc[1];
       const int64_t out_row =
           ((int64_t(cd.layer) * p.Bt + cd.b) * p.Hq + cd.kvh * kGroup + 2 * qd) * kHeadDim + 8 * g;
@@ -953,7 +1102,8 @@ __global__ void __launch_bounds__(kWarps * 32, 4) attn_kernel(const __grid_const
 struct DeviceCache {
   int dev = -1;
   int sms = 0;
-  int attn_blocks_per_sm = 0;
+  int attn_blocks_per_sm = 0;  // of the selected path
+  bool fma = false;            // GK_ATTN_PATH=fma selects the FMA comparison path
   bool attrs_set = false;
 };
 static DeviceCache g_cache[64];
@@ -967,14 +1117,21 @@ static cudaError_t device_setup(DeviceCache** out) {
   if (!c.attrs_set) {
     e = cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kAttnSmem));
+    const char* path = getenv("GK_ATTN_PATH");
+    c.fma = path != nullptr && strcmp(path, "fma") == 0;
+    e = cudaFuncSetAttribute(attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(attn_smem<true>()));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(attn_smem<false>()));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(2 * kMaxBatch * sizeof(int32_t)));
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.attn_blocks_per_sm, attn_kernel,
-                                                      kWarps * 32, kAttnSmem);
+    e = c.fma ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                    &c.attn_blocks_per_sm, attn_kernel<false>, kWarps * 32, attn_smem<false>())
+              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                    &c.attn_blocks_per_sm, attn_kernel<true>, kWarps * 32, attn_smem<true>());
     if (e != cudaSuccess) return e;
     if (c.attn_blocks_per_sm < 1) c.attn_blocks_per_sm = 1;
     c.dev = dev;
@@ -1037,11 +1194,12 @@ cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaSt
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(c->sms * c->attn_blocks_per_sm));
   cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = kAttnSmem;
+  cfg.dynamicSmemBytes = c->fma ? attn_smem<false>() : attn_smem<true>();
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_kernel, p);
+  return c->fma ? cudaLaunchKernelEx(&cfg, attn_kernel<false>, p)
+                : cudaLaunchKernelEx(&cfg, attn_kernel<true>, p);
 }
 
 cudaError_t read_device_error(cudaStream_t st, uint32_t* bits, bool clear) {
