@@ -65,7 +65,8 @@ typedef enum {
     GK_ERR_UNSUPPORTED = 2,   /* valid shape outside what this version implements */
     GK_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small */
     GK_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
-    GK_ERR_DEVICE_BOUNDS = 5  /* gk_read_device_error found a device-side error bit */
+    GK_ERR_DEVICE_BOUNDS = 5, /* gk_read_device_error found a device-side error bit */
+    GK_ERR_BUDGET = 6         /* gk_kv_budget: the KV budget is below the minimum */
 } gk_status;
 
 /* Device error-word bits (gk_read_device_error). */
@@ -191,6 +192,30 @@ gk_status gk_e4m3_quantize(const float *x, float scale, uint8_t *codes, int64_t 
  * Returns GK_ERR_DEVICE_BOUNDS when any bit was set, GK_OK otherwise.
  */
 gk_status gk_read_device_error(void *stream, uint32_t *bits, int clear);
+
+/*
+ * gk_kv_budget -- size the KV pool (host only; no GPU call).
+ * ("determine_available_memory design", sections "Heuristic formula" and
+ * "Minimum KV guard"; "GPT-OSS-120B giga-kernel decode", section "KV budget".)
+ *
+ *   total_budget = floor(total_bytes * gpu_memory_utilization)
+ *   kv_budget    = max(total_budget - used_bytes, 0)
+ *   cap          = floor(total_budget * cap_fraction)      (cap_fraction 0.30 by default on
+ *                                                            the page; 1.0 = no cap)
+ *   available    = max(min(kv_budget, cap), 0)
+ * *available_bytes receives `available`.  If shape is not NULL, *num_blocks
+ * receives floor(available / bytes_per_block) with bytes_per_block =
+ * (num_layers/2) * 2 * num_kv_heads * block_size * head_dim (one byte per FP8
+ * element, K and V halves of every group buffer); shape->num_blocks and the
+ * table sizes are not read.  Returns GK_ERR_BUDGET when available is below
+ * min_budget_gib GiB (the page's minimum-KV guard, 1.0 by default) or yields
+ * fewer than 2 blocks (one usable block plus the padding block); both outputs
+ * are still written.  GK_ERR_INVALID_ARG for gmu or cap_fraction outside
+ * (0, 1], negative min_budget_gib, or null outputs.
+ */
+gk_status gk_kv_budget(uint64_t total_bytes, uint64_t used_bytes, double gpu_memory_utilization,
+                       double cap_fraction, double min_budget_gib, const gk_shape *shape,
+                       uint64_t *available_bytes, int64_t *num_blocks);
 
 /* Human-readable name of a status code (static string). */
 const char *gk_status_str(gk_status status);

@@ -8,7 +8,7 @@ on a CUDA device, the calls raise.
 The functions carry the C names: ``gk_kv_append``, ``gk_decode_attn_stack``,
 ``gk_decode_attn_stack_static``,
 ``gk_attn_workspace_bytes``, ``gk_attn_workspace_min_bytes``,
-``gk_e4m3_quantize``, ``gk_read_device_error``, ``gk_status_str``,
+``gk_e4m3_quantize``, ``gk_kv_budget``, ``gk_read_device_error``, ``gk_status_str``,
 ``gk_abi_version``.  Tensors are torch tensors; the stream defaults to torch's
 current stream on the tensors' device.
 """
@@ -23,7 +23,7 @@ from typing import Optional, Sequence
 from . import build as _build
 
 GK_OK, GK_ERR_INVALID_ARG, GK_ERR_UNSUPPORTED, GK_ERR_WORKSPACE, GK_ERR_CUDA, \
-    GK_ERR_DEVICE_BOUNDS = range(6)
+    GK_ERR_DEVICE_BOUNDS, GK_ERR_BUDGET = range(7)
 GK_DEVERR_SLOT, GK_DEVERR_BLOCK, GK_DEVERR_POS, GK_DEVERR_TIMEOUT, GK_DEVERR_PLAN = \
     0x1, 0x2, 0x4, 0x8, 0x10
 
@@ -84,6 +84,11 @@ def lib(build_if_needed: bool = True) -> ctypes.CDLL:
             L.gk_decode_attn_stack_static.argtypes = [sp] + [vp] * 15
             L.gk_e4m3_quantize.restype = ctypes.c_int
             L.gk_e4m3_quantize.argtypes = [vp, ctypes.c_float, vp, i64, vp]
+            L.gk_kv_budget.restype = ctypes.c_int
+            L.gk_kv_budget.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_double,
+                                       ctypes.c_double, ctypes.c_double, sp,
+                                       ctypes.POINTER(ctypes.c_uint64),
+                                       ctypes.POINTER(ctypes.c_int64)]
             L.gk_read_device_error.restype = ctypes.c_int
             L.gk_read_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
             _lib = L
@@ -224,6 +229,22 @@ def gk_read_device_error(stream=None, clear: bool = True) -> int:
     if st not in (GK_OK, GK_ERR_DEVICE_BOUNDS):
         raise GkError(st, "gk_read_device_error")
     return int(bits.value)
+
+
+def gk_kv_budget(total_bytes: int, used_bytes: int, gpu_memory_utilization: float,
+                 cap_fraction: float = 0.30, min_budget_gib: float = 1.0, shape=None):
+    """KV pool size (host only): returns (status, available_bytes, num_blocks or None).
+    GK_ERR_BUDGET is returned, not raised, so that callers can report the
+    numbers the minimum-KV guard rejected."""
+    avail = ctypes.c_uint64(0)
+    nb = ctypes.c_int64(0)
+    sh = ctypes.byref(_as_shape(shape)) if shape is not None else None
+    st = lib().gk_kv_budget(int(total_bytes), int(used_bytes), float(gpu_memory_utilization),
+                            float(cap_fraction), float(min_budget_gib), sh, ctypes.byref(avail),
+                            ctypes.byref(nb) if shape is not None else None)
+    if st not in (GK_OK, GK_ERR_BUDGET):
+        raise GkError(st, "gk_kv_budget")
+    return st, int(avail.value), (int(nb.value) if shape is not None else None)
 
 
 def split_group_buffers(bufs: Sequence):

@@ -98,6 +98,7 @@ const char* gk_status_str(gk_status st) {
     case GK_ERR_WORKSPACE: return "GK_ERR_WORKSPACE";
     case GK_ERR_CUDA: return "GK_ERR_CUDA";
     case GK_ERR_DEVICE_BOUNDS: return "GK_ERR_DEVICE_BOUNDS";
+    case GK_ERR_BUDGET: return "GK_ERR_BUDGET";
   }
   return "GK_ERR_UNKNOWN";
 }
@@ -227,6 +228,32 @@ gk_status gk_decode_attn_stack(const gk_shape* shape, const void* q, void* const
   pl.max_tokens_swa = shape->max_blocks_swa * shape->block_size;
   return launch_attention(pl, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GK_OK
                                                                                    : GK_ERR_CUDA;
+}
+
+gk_status gk_kv_budget(uint64_t total_bytes, uint64_t used_bytes, double gmu, double cap_fraction,
+                       double min_budget_gib, const gk_shape* shape, uint64_t* available_bytes,
+                       int64_t* num_blocks) {
+  if (!available_bytes || (shape && !num_blocks)) return GK_ERR_INVALID_ARG;
+  if (!(gmu > 0.0 && gmu <= 1.0) || !(cap_fraction > 0.0 && cap_fraction <= 1.0) ||
+      !(min_budget_gib >= 0.0))
+    return GK_ERR_INVALID_ARG;
+  // integer truncation of the double products, as the page's int() does
+  const uint64_t total_budget = uint64_t(double(total_bytes) * gmu);
+  const uint64_t kv_budget = total_budget > used_bytes ? total_budget - used_bytes : 0;
+  const uint64_t cap = uint64_t(double(total_budget) * cap_fraction);
+  const uint64_t available = kv_budget < cap ? kv_budget : cap;
+  *available_bytes = available;
+  bool too_small = double(available) < min_budget_gib * 1073741824.0;
+  if (shape) {
+    if (shape->num_layers < 2 || (shape->num_layers & 1) || shape->num_kv_heads < 1 ||
+        shape->block_size < 1 || shape->head_dim < 1)
+      return GK_ERR_INVALID_ARG;
+    const uint64_t per_block = uint64_t(shape->num_layers / 2) * 2 * uint64_t(shape->num_kv_heads) *
+                               uint64_t(shape->block_size) * uint64_t(shape->head_dim);
+    *num_blocks = int64_t(available / per_block);
+    too_small = too_small || *num_blocks < 2;
+  }
+  return too_small ? GK_ERR_BUDGET : GK_OK;
 }
 
 gk_status gk_e4m3_quantize(const float* x, float scale, uint8_t* codes, int64_t n, void* stream) {

@@ -10,7 +10,7 @@ import paged_fp8_kv_gk_gb300 as gk
 
 EXPECTED = {"gk_kv_append", "gk_attn_workspace_bytes", "gk_attn_workspace_min_bytes",
             "gk_decode_attn_stack", "gk_e4m3_quantize", "gk_read_device_error",
-            "gk_status_str", "gk_abi_version", "gk_decode_attn_stack_static"}
+            "gk_status_str", "gk_abi_version", "gk_decode_attn_stack_static", "gk_kv_budget"}
 
 
 def test_header_declares_the_boundary():
@@ -26,9 +26,9 @@ def test_library_exports_every_declared_symbol():
 
 def test_version_and_status_strings():
     assert gk.gk_abi_version() == 1
-    names = [gk.gk_status_str(i) for i in range(6)]
+    names = [gk.gk_status_str(i) for i in range(7)]
     assert names == ["GK_OK", "GK_ERR_INVALID_ARG", "GK_ERR_UNSUPPORTED", "GK_ERR_WORKSPACE",
-                     "GK_ERR_CUDA", "GK_ERR_DEVICE_BOUNDS"]
+                     "GK_ERR_CUDA", "GK_ERR_DEVICE_BOUNDS", "GK_ERR_BUDGET"]
     assert gk.gk_status_str(99) == "GK_ERR_UNKNOWN"
 
 
