@@ -324,10 +324,23 @@ def run_gk(args):
                                 ctl["sin"], ctl["bt_full"], ctl["bt_swa"], ctl["pos"],
                                 ctl["pos_w"], ctl["active"], out, None, ws, stream=sh)
 
+    def fused_step():
+        gk.gk_decode_step(shape, q, k_new, v_new, ctl["cos"], ctl["sin"], ctl["k_scale"],
+                          ctl["v_scale"], ctl["upd_full"], ctl["upd_swa"], ctl["bt_full"],
+                          ctl["bt_swa"], ctl["pos"], ctl["pos_w"], ctl["active"], kb, vb, out,
+                          None, ws, stream=sh)
+
+    if args.step == "fused":
+        def one_step():
+            fused_step()
+    else:
+        def one_step():
+            append()
+            attention()
+
     K, W = args.steps, args.warmup
     for _ in range(W):
-        append()
-        attention()
+        one_step()
     torch.cuda.synchronize(dev)
     if gk.gk_read_device_error() != 0:
         raise RuntimeError("device error word set during warm-up")
@@ -344,8 +357,7 @@ def run_gk(args):
     clocks.mark_begin()
     ev0.record(stream)
     for k in range(K):
-        append()
-        attention()
+        one_step()
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     clocks.mark_end()
@@ -413,7 +425,8 @@ def run_gk(args):
         "e2e": {"value": round(e2e_units / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "ms_per_step": round(e2e_ms / K, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * K,  # per timed step: append, planner, attention
+        "step_form": args.step,
+        "gpu_launches": (2 if args.step == "fused" else 3) * K,  # per timed step
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -499,6 +512,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle CPU time for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step", choices=["split", "fused"], default="split",
+                    help="split: gk_kv_append + gk_decode_attn_stack; fused: gk_decode_step")
     ap.add_argument("--ws-min", action="store_true",
                     help="use the minimum attention workspace (no split-KV chunks)")
     args = ap.parse_args(argv)

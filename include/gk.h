@@ -147,6 +147,30 @@ gk_status gk_decode_attn_stack(const gk_shape *shape, const void *q, void *const
                                void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * gk_decode_step -- the whole decode step in one attention launch:
+ * gk_kv_append followed by gk_decode_attn_stack, with the same arguments and
+ * results (KV bytes identical to gk_kv_append's, outputs to
+ * gk_decode_attn_stack's).  ("GPT-OSS-120B giga-kernel decode", section
+ * "Kernel contract": one program consumes the new token's K/V, both update
+ * indices and the attention-control tensors per step.)
+ * The work unit that reads a row's new token (the last split-KV chunk of each
+ * layer, row and kv head) computes that token's codes, stores them to the
+ * cache and uses them in place of the bytes it staged; no other unit reads
+ * those bytes.  This requires the control tensors to agree as the page builds
+ * them: upd_full[b] is the slot of position pos[b] in row b of bt_full and
+ * upd_swa[b] the slot of pos_w[b] in row b of bt_swa.  Inactive rows write
+ * nothing and output zeros.  Errors: those of gk_kv_append and
+ * gk_decode_attn_stack.
+ */
+gk_status gk_decode_step(const gk_shape *shape, const void *q, const void *k_new,
+                         const void *v_new, const float *cos, const float *sin,
+                         const float *k_scale, const float *v_scale, const int32_t *upd_full,
+                         const int32_t *upd_swa, const int32_t *bt_full, const int32_t *bt_swa,
+                         const int32_t *pos, const int32_t *pos_w, const uint8_t *active,
+                         void *const *k_bufs, void *const *v_bufs, void *out, float *out_f32,
+                         void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * gk_decode_attn_stack_static -- gk_decode_attn_stack without a caller
  * workspace.  (No counterpart on the pages: an addition of this library.)
  *

@@ -6,7 +6,7 @@ is no CPU fallback: if the library cannot be built or loaded, or a tensor is not
 on a CUDA device, the calls raise.
 
 The functions carry the C names: ``gk_kv_append``, ``gk_decode_attn_stack``,
-``gk_decode_attn_stack_static``,
+``gk_decode_step``, ``gk_decode_attn_stack_static``,
 ``gk_attn_workspace_bytes``, ``gk_attn_workspace_min_bytes``,
 ``gk_e4m3_quantize``, ``gk_kv_budget``, ``gk_read_device_error``, ``gk_status_str``,
 ``gk_abi_version``.  Tensors are torch tensors; the stream defaults to torch's
@@ -80,6 +80,8 @@ def lib(build_if_needed: bool = True) -> ctypes.CDLL:
             L.gk_attn_workspace_min_bytes.argtypes = [sp]
             L.gk_decode_attn_stack.restype = ctypes.c_int
             L.gk_decode_attn_stack.argtypes = [sp] + [vp] * 15 + [sz, vp]
+            L.gk_decode_step.restype = ctypes.c_int
+            L.gk_decode_step.argtypes = [sp] + [vp] * 19 + [sz, vp]
             L.gk_decode_attn_stack_static.restype = ctypes.c_int
             L.gk_decode_attn_stack_static.argtypes = [sp] + [vp] * 15
             L.gk_e4m3_quantize.restype = ctypes.c_int
@@ -189,6 +191,29 @@ def gk_decode_attn_stack(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, b
         _ptr(out_f32, torch.float32, "out_f32", allow_none=True),
         _ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()), _stream(stream, q))
     _check(st, "gk_decode_attn_stack")
+
+
+def gk_decode_step(shape, q, k_new, v_new, cos, sin, k_scale, v_scale, upd_full, upd_swa,
+                   bt_full, bt_swa, pos, pos_w, active, k_bufs, v_bufs, out, out_f32=None,
+                   workspace=None, stream=None) -> None:
+    """gk_kv_append + gk_decode_attn_stack in one attention launch."""
+    import torch
+    sh = _as_shape(shape)
+    if workspace is None:
+        raise ValueError("workspace is required (size: gk_attn_workspace_bytes(shape))")
+    st = lib().gk_decode_step(
+        ctypes.byref(sh), _ptr(q, torch.bfloat16, "q"), _ptr(k_new, torch.bfloat16, "k_new"),
+        _ptr(v_new, torch.bfloat16, "v_new"), _ptr(cos, torch.float32, "cos"),
+        _ptr(sin, torch.float32, "sin"), _ptr(k_scale, torch.float32, "k_scale"),
+        _ptr(v_scale, torch.float32, "v_scale"), _ptr(upd_full, torch.int32, "upd_full"),
+        _ptr(upd_swa, torch.int32, "upd_swa"), _ptr(bt_full, torch.int32, "bt_full"),
+        _ptr(bt_swa, torch.int32, "bt_swa"), _ptr(pos, torch.int32, "pos"),
+        _ptr(pos_w, torch.int32, "pos_w"), _ptr(active, torch.uint8, "active"),
+        ctypes.cast(_ptr_array(k_bufs, "k_bufs"), ctypes.c_void_p),
+        ctypes.cast(_ptr_array(v_bufs, "v_bufs"), ctypes.c_void_p),
+        _ptr(out, torch.bfloat16, "out"), _ptr(out_f32, torch.float32, "out_f32", allow_none=True),
+        _ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()), _stream(stream, q))
+    _check(st, "gk_decode_step")
 
 
 def gk_decode_attn_stack_static(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, bt_full,

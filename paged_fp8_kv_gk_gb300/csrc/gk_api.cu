@@ -154,12 +154,26 @@ size_t gk_attn_workspace_min_bytes(const gk_shape* shape) {
   return L.total;
 }
 
-gk_status gk_decode_attn_stack(const gk_shape* shape, const void* q, void* const* k_bufs,
-                               void* const* v_bufs, const float* k_scale, const float* v_scale,
-                               const float* cos, const float* sin, const int32_t* bt_full,
-                               const int32_t* bt_swa, const int32_t* pos, const int32_t* pos_w,
-                               const uint8_t* active, void* out, float* out_f32, void* workspace,
-                               size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace gk {
+
+struct AppendInputs {
+  const void* k_new;
+  const void* v_new;
+  const int32_t* upd_full;
+  const int32_t* upd_swa;
+};
+
+// Validation and launch shared by gk_decode_attn_stack and gk_decode_step
+// (app != nullptr: the fused step, where the units append the new token).
+static gk_status decode_attention(const gk_shape* shape, const void* q, void* const* k_bufs,
+                                  void* const* v_bufs, const float* k_scale, const float* v_scale,
+                                  const float* cos, const float* sin, const int32_t* bt_full,
+                                  const int32_t* bt_swa, const int32_t* pos, const int32_t* pos_w,
+                                  const uint8_t* active, void* out, float* out_f32,
+                                  void* workspace, size_t ws_bytes, void* stream,
+                                  const AppendInputs* app) {
   const gk_status st = check_shape(shape);
   if (st != GK_OK) return st;
   if (!q || !k_bufs || !v_bufs || !k_scale || !v_scale || !cos || !sin || !bt_full || !bt_swa ||
@@ -167,6 +181,9 @@ gk_status gk_decode_attn_stack(const gk_shape* shape, const void* q, void* const
     return GK_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(out) || (out_f32 && !aligned16(out_f32)) || !aligned16(cos) ||
       !aligned16(sin))
+    return GK_ERR_INVALID_ARG;
+  if (app && (!app->k_new || !app->v_new || !app->upd_full || !app->upd_swa ||
+              !aligned16(app->k_new) || !aligned16(app->v_new)))
     return GK_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return GK_ERR_WORKSPACE;
   const WsLayout L = ws_layout(*shape, ws_bytes);
@@ -181,6 +198,13 @@ gk_status gk_decode_attn_stack(const gk_shape* shape, const void* q, void* const
       return GK_ERR_INVALID_ARG;
     p.kb[j] = static_cast<const uint8_t*>(k_bufs[j]);
     p.vb[j] = static_cast<const uint8_t*>(v_bufs[j]);
+  }
+  if (app) {
+    p.fused = 1;
+    p.k_new = static_cast<const uint16_t*>(app->k_new);
+    p.v_new = static_cast<const uint16_t*>(app->v_new);
+    p.upd_full = app->upd_full;
+    p.upd_swa = app->upd_swa;
   }
   p.q = static_cast<const uint16_t*>(q);
   p.out = static_cast<uint16_t*>(out);
@@ -228,6 +252,32 @@ gk_status gk_decode_attn_stack(const gk_shape* shape, const void* q, void* const
   pl.max_tokens_swa = shape->max_blocks_swa * shape->block_size;
   return launch_attention(pl, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GK_OK
                                                                                    : GK_ERR_CUDA;
+}
+
+}  // namespace gk
+
+extern "C" {
+
+gk_status gk_decode_attn_stack(const gk_shape* shape, const void* q, void* const* k_bufs,
+                               void* const* v_bufs, const float* k_scale, const float* v_scale,
+                               const float* cos, const float* sin, const int32_t* bt_full,
+                               const int32_t* bt_swa, const int32_t* pos, const int32_t* pos_w,
+                               const uint8_t* active, void* out, float* out_f32, void* workspace,
+                               size_t ws_bytes, void* stream) {
+  return decode_attention(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, bt_full, bt_swa,
+                          pos, pos_w, active, out, out_f32, workspace, ws_bytes, stream, nullptr);
+}
+
+gk_status gk_decode_step(const gk_shape* shape, const void* q, const void* k_new,
+                         const void* v_new, const float* cos, const float* sin,
+                         const float* k_scale, const float* v_scale, const int32_t* upd_full,
+                         const int32_t* upd_swa, const int32_t* bt_full, const int32_t* bt_swa,
+                         const int32_t* pos, const int32_t* pos_w, const uint8_t* active,
+                         void* const* k_bufs, void* const* v_bufs, void* out, float* out_f32,
+                         void* workspace, size_t ws_bytes, void* stream) {
+  const AppendInputs app = {k_new, v_new, upd_full, upd_swa};
+  return decode_attention(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, bt_full, bt_swa,
+                          pos, pos_w, active, out, out_f32, workspace, ws_bytes, stream, &app);
 }
 
 gk_status gk_kv_budget(uint64_t total_bytes, uint64_t used_bytes, double gmu, double cap_fraction,

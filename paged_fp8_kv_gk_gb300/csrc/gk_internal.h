@@ -91,6 +91,12 @@ struct AttnParams {
   int32_t* tickets;
   float* partials;
   int64_t cap;  // partial records per (layer pair, kv head) plane
+  // fused step (gk_decode_step): the unit holding the new token appends it first
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const int32_t* upd_full;
+  const int32_t* upd_swa;
+  int fused;
   int NL, Bt, Hq, Hkv, B, nb, W, MBF, MBS;
 };
 

@@ -51,6 +51,43 @@ __device__ __forceinline__ float div_scale(float x, float s, float r) {
 // per group rather than a chain of dependent ones).
 constexpr int kAppendHeads = 8;
 
+// The append of one (layer, row, kv head) by one warp, the same arithmetic as
+// kv_append_kernel: lane l rotates the pair (l, l + 32) of k and converts
+// channels 2l, 2l + 1 of v.  Returns false (and sets the error bit) when the
+// update slot lies outside the buffer.
+__device__ __forceinline__ bool append_one(const uint16_t* k_new, const uint16_t* v_new,
+                                           const float* cosb, const float* sinb,
+                                           const float* k_scale, const float* v_scale,
+                                           const int32_t* upd_full, const int32_t* upd_swa,
+                                           uint8_t* kbuf, uint8_t* vbuf, int Bt, int Hkv, int B,
+                                           int nb, int i, int b, int h, int lane) {
+  const int32_t slot = (i & 1) ? upd_full[b] : upd_swa[b];
+  if (slot < 0 || int64_t(slot) >= int64_t(nb) * B) {
+    if (lane == 0) set_error(GK_DEVERR_SLOT);
+    return false;
+  }
+  const int64_t pb = slot / B;
+  const int t = slot % B;
+  const int64_t row = (int64_t(i) * Bt + b) * Hkv + h;
+  const float x = __uint_as_float(uint32_t(k_new[row * kHeadDim + lane]) << 16);
+  const float y = __uint_as_float(uint32_t(k_new[row * kHeadDim + lane + 32]) << 16);
+  const uint32_t vw = reinterpret_cast<const uint32_t*>(v_new + row * kHeadDim)[lane];
+  const float c = cosb[b * (kHeadDim / 2) + lane];
+  const float s = sinb[b * (kHeadDim / 2) + lane];
+  const float ks = k_scale[i], vs = v_scale[i];
+  const float kr_inv = exact_reciprocal(ks), vr_inv = exact_reciprocal(vs);
+  const float xr = __fsub_rn(__fmul_rn(x, c), __fmul_rn(y, s));
+  const float yr = __fadd_rn(__fmul_rn(y, c), __fmul_rn(x, s));
+  const uint32_t kc = f32x2_to_e4m3x2(div_scale(xr, ks, kr_inv), div_scale(yr, ks, kr_inv));
+  uint8_t* kdst = kbuf + ((pb * Hkv + h) * (B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1);
+  kdst[2 * lane] = uint8_t(kc & 0xffu);
+  kdst[2 * (lane + 32)] = uint8_t(kc >> 8);
+  const uint32_t vc = f32x2_to_e4m3x2(div_scale(bf16lo_to_f32(vw), vs, vr_inv),
+                                      div_scale(bf16hi_to_f32(vw), vs, vr_inv));
+  reinterpret_cast<uint16_t*>(vbuf + ((pb * Hkv + h) * B + t) * kHeadDim)[lane] = uint16_t(vc);
+  return true;
+}
+
 __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ AppendParams p) {
   // The decode-attention planner may launch now: it reads only positions and
   // the active mask, and waits for this grid before it exits.
@@ -389,6 +426,7 @@ struct UnitDesc {
   int32_t layer, b, kvh, s, ns;
   int32_t t_begin, t_end;  // key range [t_begin, t_end) in the table's frame
   int32_t st_begin, n_st;  // 32-token stages covering the range
+  int32_t slot;            // fused step: update slot of the unit's new token
 };
 
 // q of the unit's 8 heads (bf16) followed by its row's cos and sin (fp32),
@@ -396,6 +434,8 @@ struct UnitDesc {
 constexpr uint32_t kQBytes = kGroup * kHeadDim * 2;
 constexpr uint32_t kRopeBytes = (kHeadDim / 2) * 4;
 constexpr uint32_t kUnitHeadBytes = kQBytes + 2 * kRopeBytes;
+// fused step: the new token's k and v rows (bf16) follow the unit head
+constexpr uint32_t kNewKvBytes = 2 * kHeadDim * 2;
 
 // The FMA comparison path keeps q' in fp32 (rows padded so the eight heads
 // fall in different banks) and one stage of P for the exchange between its
@@ -407,9 +447,10 @@ constexpr int kQfStride = kHeadDim + 4;
 template <bool kMma>
 struct alignas(128) WarpSmemT {
   uint8_t ring[kStages][kStageBytes];
-  uint8_t qbuf[kUnitHeadBytes];
+  uint8_t qbuf[kUnitHeadBytes + kNewKvBytes];
   float qf[kMma ? 4 : kGroup * kQfStride];
   float pbuf[kMma ? 4 : kStageTok * kGroup];
+  uint32_t apbuf[32];  // fused step: the new token's codes per lane
   unsigned long long bar[kStages];
   UnitDesc fifo[kFifo];
 };
@@ -455,7 +496,10 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int u, int4 e, 
 // measure the choice (selected with GK_ATTN_PATH=fma).
 // 4 CTAs (16 warps) per SM: latency hiding across warps measured worth more
 // than a deeper ring or the registers above 128.
-template <bool kMma>
+// kFused = true: the decode step's append is done by the units that read the
+// new token (gk_decode_step); a separate instantiation so that the plain
+// attention kernel keeps its own register allocation.
+template <bool kMma, bool kFused>
 __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -490,6 +534,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   bool tn_ready = false;
   int32_t tbl_next = 0;
   int tbl_next_base = 0;
+  int32_t upd_next = 0;  // fused step: update slot of the next unit's row and layer
   // lane l: entry l of the table chunk starting at the unit's first block
   auto load_tbl = [&](int4 e, int& base) -> int32_t {
     const bool swa = ((e.w >> 30) & 1) != 0;
@@ -510,6 +555,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   int32_t tbl = 0;
   bool failed = false;
   bool q_free = true;  // the q buffer may take the next unit's q
+  bool pu_appends = false;  // fused step: the producer's unit carries the new token
 
   // lane 0: copy the producer unit's q (8 heads) and its row's cos/sin rows
   auto issue_unit_head = [&](uint32_t bar) {
@@ -518,6 +564,11 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     bulk_g2s(qbuf0, qsrc, kQBytes, bar);
     bulk_g2s(qbuf0 + kQBytes, p.cosb + int64_t(pu_b) * (kHeadDim / 2), kRopeBytes, bar);
     bulk_g2s(qbuf0 + kQBytes + kRopeBytes, p.sinb + int64_t(pu_b) * (kHeadDim / 2), kRopeBytes, bar);
+    if (kFused && pu_appends) {
+      const int64_t row = (int64_t(pu_layer) * p.Bt + pu_b) * p.Hkv + pu_kvh;
+      bulk_g2s(qbuf0 + kUnitHeadBytes, p.k_new + row * kHeadDim, kHeadDim * 2, bar);
+      bulk_g2s(qbuf0 + kUnitHeadBytes + kHeadDim * 2, p.v_new + row * kHeadDim, kHeadDim * 2, bar);
+    }
   };
 
   // Next unit from the pipeline (warp-uniform); zero-fill units (inactive
@@ -529,12 +580,18 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       if (u >= nU + nZ) return false;
       int32_t tcur = 0;
       int tcur_base = 0;
+      int32_t ucur = 0;
       if (u < nU) {
         if (tn_ready) {
           tcur = tbl_next;
           tcur_base = tbl_next_base;
+          ucur = upd_next;
         } else {
           tcur = load_tbl(e, tcur_base);
+          if constexpr (kFused) {
+            const bool swa_u = ((e.w >> 30) & 1) != 0;
+            ucur = swa_u ? __ldg(p.upd_swa + e.x) : __ldg(p.upd_full + e.x);
+          }
         }
       }
       if (lane == 0) u_after = atomicAdd(p.queue, 1);
@@ -547,6 +604,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         continue;
       }
       decode_unit(p, u, e, planes, d);
+      d.slot = ucur;
       tbl = tcur;
       tbl_base = tcur_base;
       return true;
@@ -574,11 +632,17 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       pu_kind = d.kind;
       pu_t_end = d.t_end;
       q_free = false;
+      pu_appends = kFused && d.s == d.ns - 1;
     } else if (!tn_ready && u_next < nU) {
       tbl_next = load_tbl(e_next, tbl_next_base);
+      if constexpr (kFused) {
+        const bool swa_next = ((e_next.w >> 30) & 1) != 0;
+        upd_next = swa_next ? __ldg(p.upd_swa + e_next.x) : __ldg(p.upd_full + e_next.x);
+      }
       tn_ready = true;
     }
-    const uint32_t head_bytes = pk == 0 ? kUnitHeadBytes : 0u;
+    const uint32_t head_bytes =
+        pk == 0 ? kUnitHeadBytes + ((kFused && pu_appends) ? kNewKvBytes : 0u) : 0u;
     const int tok0 = (pu_st_begin + pk) * kStageTok;
     const int slot = prod % kStages;
     const uint32_t dst = ring0 + slot * kStageBytes;
@@ -641,7 +705,13 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   };
 
   // ------------------------------------------------ consumer state
-  UnitDesc cd;
+  // The consumer's unit: the fields the stage loop uses live in registers;
+  // the others are read from its descriptor in shared memory (the slot stays
+  // put while the unit runs: the FIFO holds more units than the ring can run ahead).
+  struct {
+    int t_begin, t_end, st_begin, n_st;
+  } cd;
+#define CU (ws.fifo[f_head % kFifo])
   int k_in_unit = 0;
   uint32_t qhi[8], qlo[8];  // q' = qhi + qlo (f16 each): ~22-bit significand
   // Scores come out of the MMA as x * 2^e_h, x = logit in log2 units and
@@ -655,6 +725,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   // FMA path: per-head reference maxima / thresholds (log2 units, warp-uniform)
   // and this lane's partial denominators (lane = token)
   float mh[kMma ? 1 : kGroup], thh[kMma ? 1 : kGroup], lsum[kMma ? 1 : kGroup];
+  // fused step: codes of the new token (lane l: k channels l, l+32; v channels
+  // 2l, 2l+1) and its update slot, computed at the unit's start
 
   while (prod - cons < kStages && issue_next()) {
   }
@@ -670,7 +742,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       break;
     }
     if (k_in_unit == 0) {
-      cd = ws.fifo[f_head % kFifo];
+      cd.t_begin = CU.t_begin;
+      cd.t_end = CU.t_end;
+      cd.st_begin = CU.st_begin;
+      cd.n_st = CU.n_st;
       // ---- unit prologue: rotated q for head (kvh*8 + g), channels 16qd..16qd+15
       const uint32_t qrow = qbuf0 + g * (kHeadDim * 2);
       const uint4 x0 = lds128(qrow + 32 * qd);
@@ -689,11 +764,39 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         cw[4 * k] = c4.x; cw[4 * k + 1] = c4.y; cw[4 * k + 2] = c4.z; cw[4 * k + 3] = c4.w;
         sw[4 * k] = s4.x; sw[4 * k + 1] = s4.y; sw[4 * k + 2] = s4.z; sw[4 * k + 3] = s4.w;
       }
+      if constexpr (kFused) {
+        if (CU.s == CU.ns - 1) {
+          // the same arithmetic as gk_kv_append, from the rows the head copy brought
+          const uint32_t kr = qbuf0 + kUnitHeadBytes;
+          uint16_t kx16, ky16;
+          asm volatile("ld.shared.u16 %0, [%1];" : "=h"(kx16) : "r"(kr + 2 * lane));
+          asm volatile("ld.shared.u16 %0, [%1];" : "=h"(ky16) : "r"(kr + 2 * (lane + 32)));
+          uint32_t vw, cb, sb;
+          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(vw) : "r"(kr + kHeadDim * 2 + 4 * lane));
+          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(cb) : "r"(qbuf0 + kQBytes + 4 * lane));
+          asm volatile("ld.shared.u32 %0, [%1];"
+                       : "=r"(sb)
+                       : "r"(qbuf0 + kQBytes + kRopeBytes + 4 * lane));
+          const float x = __uint_as_float(uint32_t(kx16) << 16);
+          const float y = __uint_as_float(uint32_t(ky16) << 16);
+          const float c = __uint_as_float(cb), sn = __uint_as_float(sb);
+          const float ks = p.k_scale[CU.layer], vs = p.v_scale[CU.layer];
+          const float kr_inv = exact_reciprocal(ks), vr_inv = exact_reciprocal(vs);
+          const float xr = __fsub_rn(__fmul_rn(x, c), __fmul_rn(y, sn));
+          const float yr = __fadd_rn(__fmul_rn(y, c), __fmul_rn(x, sn));
+          // k codes in the low half, v codes in the high half, kept to the last stage
+          ws.apbuf[lane] =
+              f32x2_to_e4m3x2(div_scale(xr, ks, kr_inv), div_scale(yr, ks, kr_inv)) |
+              (f32x2_to_e4m3x2(div_scale(bf16lo_to_f32(vw), vs, vr_inv),
+                               div_scale(bf16hi_to_f32(vw), vs, vr_inv))
+               << 16);
+        }
+      }
       __syncwarp();
       q_free = true;
       const float sgn = qd < 2 ? -1.f : 1.f;
       // logits in log2 units: q'.k * k_scale / sqrt(D) * log2(e), folded into q
-      const float ck = p.k_scale[cd.layer] * (0.125f * 1.4426950408889634f);
+      const float ck = p.k_scale[CU.layer] * (0.125f * 1.4426950408889634f);
       float r[16];
       float amax = 0.f;
 #pragma unroll
@@ -738,7 +841,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         si0 = __shfl_sync(kFull, finv, 8 * qd);   // heads 2qd and 2qd+1
         si1 = __shfl_sync(kFull, finv, 8 * qd + 4);
       }
-      vscale = p.v_scale[cd.layer];
+      vscale = p.v_scale[CU.layer];
       mr0 = mr1 = thr0 = thr1 = -INFINITY;
       nb0 = nb1 = 0.f;
       lacc[0] = lacc[1] = lacc[2] = lacc[3] = 0.f;
@@ -750,6 +853,36 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     const uint32_t Vs = Ks + kStageKBytes;
     const int tok0 = (cd.st_begin + k_in_unit) * kStageTok;
     const bool edge = tok0 < cd.t_begin || tok0 + kStageTok > cd.t_end;
+    if constexpr (kFused) {
+      if (k_in_unit == cd.n_st - 1 && CU.s == CU.ns - 1) {
+        // the new token is the last key of the unit: store its codes to the
+        // cache and into the staged copy (which holds the bytes from before)
+        const int32_t ap_slot = CU.slot;
+        const uint32_t ap_codes = ws.apbuf[lane];
+        if (ap_slot < 0 || int64_t(ap_slot) >= int64_t(p.nb) * p.B) {
+          if (lane == 0) set_error(GK_DEVERR_SLOT);
+        } else {
+          const int64_t pb = ap_slot / p.B;
+          const int t = ap_slot % p.B;
+          uint8_t* kdst = const_cast<uint8_t*>(p.kb[CU.layer >> 1]) +
+                          ((pb * p.Hkv + CU.kvh) * (p.B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1);
+          kdst[2 * lane] = uint8_t(ap_codes & 0xffu);
+          kdst[2 * (lane + 32)] = uint8_t((ap_codes >> 8) & 0xffu);
+          uint8_t* vdst = const_cast<uint8_t*>(p.vb[CU.layer >> 1]) +
+                          ((pb * p.Hkv + CU.kvh) * p.B + t) * kHeadDim;
+          reinterpret_cast<uint16_t*>(vdst)[lane] = uint16_t(ap_codes >> 16);
+          const int tl = cd.t_end - 1 - tok0;
+          const uint32_t kp = Ks + (tl >> 1) * (2 * kHeadDim) + (tl & 1);
+          const uint16_t k0 = uint16_t(ap_codes & 0xffu), k1 = uint16_t((ap_codes >> 8) & 0xffu);
+          asm volatile("st.shared.u8 [%0], %1;" ::"r"(kp + 2 * lane), "h"(k0) : "memory");
+          asm volatile("st.shared.u8 [%0], %1;" ::"r"(kp + 2 * (lane + 32)), "h"(k1) : "memory");
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(Vs + tl * kHeadDim + 2 * lane),
+                       "h"(uint16_t(ap_codes >> 16))
+                       : "memory");
+        }
+        __syncwarp();
+      }
+    }
 
     if constexpr (kMma) {
     // ---- S = q' K^T for two 16-token tiles; rows (g, g+8) = tokens (2p, 2p+1)
@@ -951,7 +1084,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     if (k_in_unit == cd.n_st) {
       // ---- unit epilogue
       k_in_unit = 0;
-      ++f_head;
       if constexpr (!kMma) {
 #pragma unroll
         for (int h = 0; h < kGroup; ++h) {
@@ -969,8 +1101,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       }
       const float l0 = lacc[0], l1 = lacc[1];
       const int64_t out_row =
-          ((int64_t(cd.layer) * p.Bt + cd.b) * p.Hq + cd.kvh * kGroup + 2 * qd) * kHeadDim + 8 * g;
-      if (cd.ns == 1) {
+          ((int64_t(CU.layer) * p.Bt + CU.b) * p.Hq + CU.kvh * kGroup + 2 * qd) * kHeadDim + 8 * g;
+      if (CU.ns == 1) {
         const float i0 = vscale / l0, i1 = vscale / l1;
         float r0[8], r1[8];
 #pragma unroll
@@ -1001,10 +1133,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         }
       } else {
         // split partial: (m, l, o) unnormalised, in log2 units
-        const int j = cd.layer >> 1;
-        const int64_t plane = int64_t(j) * p.Hkv + cd.kvh;
+        const int j = CU.layer >> 1;
+        const int64_t plane = int64_t(j) * p.Hkv + CU.kvh;
         const int64_t cap = p.cap;
-        float* rec = p.partials + ((plane * cap) + p.part_base[cd.b] + cd.s) * kPartialFloats;
+        float* rec = p.partials + ((plane * cap) + p.part_base[CU.b] + CU.s) * kPartialFloats;
         if (g == 0) {
           rec[2 * qd] = mr0 * si0;  // log2 units
           rec[2 * qd + 1] = mr1 * si1;
@@ -1020,18 +1152,18 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         __threadfence();
         __syncwarp();
         int old = 0;
-        int32_t* ticket = p.tickets + (int64_t(j) * p.Bt + cd.b) * p.Hkv + cd.kvh;
+        int32_t* ticket = p.tickets + (int64_t(j) * p.Bt + CU.b) * p.Hkv + CU.kvh;
         if (lane == 0) old = atomicAdd(ticket, 1);
         old = __shfl_sync(kFull, old, 0);
-        if (old == cd.ns - 1) {
+        if (old == CU.ns - 1) {
           // last split to finish: merge all of this row's partials in split order
           __threadfence();
-          const float* base = p.partials + (plane * cap + p.part_base[cd.b]) * kPartialFloats;
+          const float* base = p.partials + (plane * cap + p.part_base[CU.b]) * kPartialFloats;
           float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
           float a0[8], a1[8];
 #pragma unroll
           for (int c = 0; c < 8; ++c) a0[c] = a1[c] = 0.f;
-          for (int s = 0; s < cd.ns; ++s) {
+          for (int s = 0; s < CU.ns; ++s) {
             const float* rs = base + int64_t(s) * kPartialFloats;
             const float ms0 = ldg_cg_f(rs + 2 * qd), ms1 = ldg_cg_f(rs + 2 * qd + 1);
             const float ls0 = ldg_cg_f(rs + kGroup + 2 * qd), ls1 = ldg_cg_f(rs + kGroup + 2 * qd + 1);
@@ -1081,9 +1213,11 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
           }
         }
       }
+      ++f_head;
     }
   }
 
+#undef CU
   if (failed) {
     // A barrier wait hit its limit: record it, then wait (bounded) for this
     // warp's copies still in flight before the CTA may exit.
@@ -1119,19 +1253,32 @@ static cudaError_t device_setup(DeviceCache** out) {
     if (e != cudaSuccess) return e;
     const char* path = getenv("GK_ATTN_PATH");
     c.fma = path != nullptr && strcmp(path, "fma") == 0;
-    e = cudaFuncSetAttribute(attn_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(attn_smem<true>()));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(attn_smem<false>()));
-    if (e != cudaSuccess) return e;
+    const void* kernels[4] = {(const void*)attn_kernel<true, false>,
+                              (const void*)attn_kernel<true, true>,
+                              (const void*)attn_kernel<false, false>,
+                              (const void*)attn_kernel<false, true>};
+    for (int k = 0; k < 4; ++k) {
+      e = cudaFuncSetAttribute(kernels[k], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(k < 2 ? attn_smem<true>() : attn_smem<false>()));
+      if (e != cudaSuccess) return e;
+    }
     e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(2 * kMaxBatch * sizeof(int32_t)));
     if (e != cudaSuccess) return e;
+    // both instantiations of a path are launched with the occupancy of the
+    // plain one; the fused one must fit the same number of CTAs
+    int fused_blocks = 0;
     e = c.fma ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                    &c.attn_blocks_per_sm, attn_kernel<false>, kWarps * 32, attn_smem<false>())
+                    &c.attn_blocks_per_sm, attn_kernel<false, false>, kWarps * 32, attn_smem<false>())
               : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                    &c.attn_blocks_per_sm, attn_kernel<true>, kWarps * 32, attn_smem<true>());
+                    &c.attn_blocks_per_sm, attn_kernel<true, false>, kWarps * 32, attn_smem<true>());
+    if (e != cudaSuccess) return e;
+    e = c.fma ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                    &fused_blocks, attn_kernel<false, true>, kWarps * 32, attn_smem<false>())
+              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                    &fused_blocks, attn_kernel<true, true>, kWarps * 32, attn_smem<true>());
+    if (e != cudaSuccess) return e;
+    if (fused_blocks < c.attn_blocks_per_sm) c.attn_blocks_per_sm = fused_blocks;
     if (e != cudaSuccess) return e;
     if (c.attn_blocks_per_sm < 1) c.attn_blocks_per_sm = 1;
     c.dev = dev;
@@ -1198,8 +1345,11 @@ cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaSt
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return c->fma ? cudaLaunchKernelEx(&cfg, attn_kernel<false>, p)
-                : cudaLaunchKernelEx(&cfg, attn_kernel<true>, p);
+  if (p.fused)
+    return c->fma ? cudaLaunchKernelEx(&cfg, attn_kernel<false, true>, p)
+                  : cudaLaunchKernelEx(&cfg, attn_kernel<true, true>, p);
+  return c->fma ? cudaLaunchKernelEx(&cfg, attn_kernel<false, false>, p)
+                : cudaLaunchKernelEx(&cfg, attn_kernel<true, false>, p);
 }
 
 cudaError_t read_device_error(cudaStream_t st, uint32_t* bits, bool clear) {

@@ -83,6 +83,14 @@ class GpuStep:
                         self.v_scale, self.upd_full, self.upd_swa, self.active, self.kb, self.vb,
                         stream=stream)
 
+    def step(self, workspace=None, out_f32=True, stream=None):
+        """The fused step (gk_decode_step): append + attention in one launch."""
+        gk.gk_decode_step(self.shape, self.q, self.k_new, self.v_new, self.cos, self.sin,
+                          self.k_scale, self.v_scale, self.upd_full, self.upd_swa, self.bt_full,
+                          self.bt_swa, self.pos, self.pos_w, self.active, self.kb, self.vb,
+                          self.out, self.out_f32 if out_f32 else None,
+                          self.workspace if workspace is None else workspace, stream=stream)
+
     def attention(self, workspace=None, out_f32=True, stream=None):
         gk.gk_decode_attn_stack(self.shape, self.q, self.kb, self.vb, self.k_scale, self.v_scale,
                                 self.cos, self.sin, self.bt_full, self.bt_swa, self.pos,
