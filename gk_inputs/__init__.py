@@ -113,6 +113,13 @@ REDUCED = {
     "swa_small_peaky": WORKLOADS["swa_b512"].replace(
         name="swa_small_peaky", num_layers=4, batch=16, lengths="uniform:64,512", seed=18,
         sigma_q=3.0),
+    # block 128 with one kv head: the page's 120B GK config seen by one TP8 rank
+    "gk120b_rank_small": WORKLOADS["tiny"].replace(
+        name="gk120b_rank_small", num_layers=4, batch=5, block_size=128,
+        lengths="fixed:1,127,128,129,700", seed=19, num_blocks=None, scale=None),
+    "block64_small": WORKLOADS["gptoss_b64"].replace(
+        name="block64_small", num_layers=4, batch=5, block_size=64,
+        lengths="fixed:1,63,64,200,1000", seed=20),
     "block16_small": WORKLOADS["tiny"].replace(
         name="block16_small", num_layers=4, batch=5, num_q_heads=16, num_kv_heads=2,
         lengths="fixed:1,15,16,143,300", seed=17, num_blocks=None),

@@ -91,6 +91,9 @@ def lib(build_if_needed: bool = True) -> ctypes.CDLL:
                                        ctypes.c_double, ctypes.c_double, sp,
                                        ctypes.POINTER(ctypes.c_uint64),
                                        ctypes.POINTER(ctypes.c_int64)]
+            L.gk_selftest_wait_timeout.restype = ctypes.c_int
+            L.gk_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp,
+                                                   ctypes.POINTER(ctypes.c_uint32)]
             L.gk_read_device_error.restype = ctypes.c_int
             L.gk_read_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
             _lib = L
@@ -270,6 +273,16 @@ def gk_kv_budget(total_bytes: int, used_bytes: int, gpu_memory_utilization: floa
     if st not in (GK_OK, GK_ERR_BUDGET):
         raise GkError(st, "gk_kv_budget")
     return st, int(avail.value), (int(nb.value) if shape is not None else None)
+
+
+def gk_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    """Test hook (include/gk_testing.h): run the bounded barrier wait into its
+    limit on the GPU; returns the device error word (GK_DEVERR_TIMEOUT expected)."""
+    bits = ctypes.c_uint32(0)
+    st = lib().gk_selftest_wait_timeout(int(limit_ns), _stream(stream), ctypes.byref(bits))
+    if st not in (GK_OK, GK_ERR_DEVICE_BOUNDS):
+        raise GkError(st, "gk_selftest_wait_timeout")
+    return int(bits.value)
 
 
 def split_group_buffers(bufs: Sequence):

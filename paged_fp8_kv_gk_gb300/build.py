@@ -41,7 +41,8 @@ def _stale() -> bool:
     if not os.path.exists(LIB_PATH):
         return True
     t = os.path.getmtime(LIB_PATH)
-    deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, "gk.h")]
+    deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [
+        os.path.join(INCLUDE, h) for h in ("gk.h", "gk_testing.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 

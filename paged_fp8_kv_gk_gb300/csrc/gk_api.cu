@@ -4,6 +4,7 @@
 #include <string.h>
 
 #include "gk_internal.h"
+#include "../../include/gk_testing.h"
 
 namespace gk {
 
@@ -311,6 +312,13 @@ gk_status gk_e4m3_quantize(const float* x, float scale, uint8_t* codes, int64_t 
   return launch_quantize(x, scale, codes, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? GK_OK
              : GK_ERR_CUDA;
+}
+
+gk_status gk_selftest_wait_timeout(uint64_t limit_ns, void* stream, uint32_t* bits) {
+  if (!bits || limit_ns < 1000ull || limit_ns > 1000000000ull) return GK_ERR_INVALID_ARG;
+  if (launch_wait_timeout(limit_ns, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GK_ERR_CUDA;
+  return gk_read_device_error(stream, bits, 1);
 }
 
 gk_status gk_read_device_error(void* stream, uint32_t* bits, int clear) {

@@ -107,5 +107,6 @@ cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaSt
 // Resident warps of the persistent attention grid on the current device.
 int attention_resident_warps();
 cudaError_t read_device_error(cudaStream_t st, uint32_t* bits, bool clear);
+cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t st);
 
 }  // namespace gk

@@ -1231,6 +1231,25 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
 }
 
 // =========================================================================
+// Test hook: the bounded barrier wait running out
+// =========================================================================
+__global__ void wait_timeout_kernel(uint64_t limit_ns) {
+  __shared__ unsigned long long bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);  // one arrival expected; none ever comes
+    mbar_init_fence();
+  }
+  __syncwarp();
+  if (!mbar_wait_bounded(b, 0, limit_ns) && threadIdx.x == 0) set_error(GK_DEVERR_TIMEOUT);
+}
+
+cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(limit_ns);
+  return cudaGetLastError();
+}
+
+// =========================================================================
 // Launchers
 // =========================================================================
 struct DeviceCache {

@@ -126,3 +126,12 @@ def test_binding_refuses_cpu_tensors():
     t = torch.zeros(16, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         gk.gk_kv_append(sh, t, t, t, t, t, t, t, t, t, [t], [t], stream=0)
+
+
+def test_testing_header_symbol_exported_and_validates():
+    L = gk.lib()
+    assert hasattr(L, "gk_selftest_wait_timeout")
+    b = ctypes.c_uint32()
+    assert L.gk_selftest_wait_timeout(10, None, ctypes.byref(b)) == gk.GK_ERR_INVALID_ARG
+    assert L.gk_selftest_wait_timeout(10 ** 10, None, ctypes.byref(b)) == gk.GK_ERR_INVALID_ARG
+    assert L.gk_selftest_wait_timeout(10 ** 6, None, None) == gk.GK_ERR_INVALID_ARG

@@ -80,7 +80,8 @@ def _brute_step(w, c, q_bits, cache):
 
 
 # ------------------------------------------------------------------ whole step
-@pytest.mark.parametrize("name", ["tiny", "block16_small", "gptoss_small", "swa_small"])
+@pytest.mark.parametrize("name", ["tiny", "block16_small", "gptoss_small", "swa_small",
+                                  "gk120b_rank_small", "block64_small"])
 def test_oracle_step_matches_independent_restatement(name):
     w, c, st, cache = _setup(name)
     q = gi.bf16_bits(st["q"])
