@@ -169,18 +169,26 @@ class ClockSampler:
                 "samples": len(use), "samples_in_timed_region": len(inside), "reasons": reasons}
 
 
-def workload_config(w, c, l2_note: str):
+def kv_layout_desc(k_layout: str = "packed", kv_form: str = "per_group") -> str:
+    form = ("per-group buffers [2,nb,kv,B,D]" if kv_form == "per_group"
+            else "stacked K_cache/V_cache [G,nb,kv,B,D]")
+    k = "K packed [..,B/2,D,2]" if k_layout == "packed" else "K unpacked [..,B,D]"
+    return f"{form}, {k}, E4M3"
+
+
+def workload_config(w, c, l2_note: str, kv_layout: str = None):
     kind, _, arg = w.lengths.partition(":")
     return {"workload": w.name, "num_layers": w.num_layers, "batch": w.batch,
             "active_rows": int(c.active.sum()), "q_heads": w.num_q_heads,
             "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
             "window": w.window, "context": f"{kind}:{arg}", "mean_context": float(c.lengths[c.active == 1].mean()),
-            "kv_layout": "per-group buffers [2,nb,kv,B,D], K packed [..,B/2,D,2], E4M3",
+            "kv_layout": kv_layout or kv_layout_desc(),
             "l2": l2_note}
 
 
 # ------------------------------------------------------------------ CPU baseline (oracle)
-def oracle_sample(w, c, step_host, cache, budget_s: float, seed: int = 0, rows_max=None):
+def oracle_sample(w, c, step_host, cache, budget_s: float, seed: int = 0, rows_max=None,
+                  k_layout: int = 0):
     """Time the oracle (single-threaded C) on whole rows of the workload: for
     each sampled row, every layer pair's append + attention for all kv heads.
     Returns (layer*seq per second, layer*seqs done, seconds, rows)."""
@@ -194,11 +202,11 @@ def oracle_sample(w, c, step_host, cache, budget_s: float, seed: int = 0, rows_m
         for j in range(w.num_layers // 2):
             ids = np.concatenate([np.asarray(c.full_blocks[b], np.int64),
                                   np.asarray(c.swa_blocks[b], np.int64)])
-            idx = torch.as_tensor(ids, device=cache[j].device)
+            idx = torch.as_tensor(ids, device=cache[j][0].device)
             kp = cache[j][0].index_select(0, idx).cpu().numpy().reshape(-1)
             vp = cache[j][1].index_select(0, idx).cpu().numpy().reshape(-1)
             t0 = time.perf_counter()
-            orows.row_pair_from_pool(w, c, step_host, kp, vp, j, b)
+            orows.row_pair_from_pool(w, c, step_host, kp, vp, j, b, k_layout=k_layout)
             spent += time.perf_counter() - t0
             done += 2
         used.append(b)
@@ -208,7 +216,7 @@ def oracle_sample(w, c, step_host, cache, budget_s: float, seed: int = 0, rows_m
 
 
 # ------------------------------------------------------------------ end-to-end loop
-def run_e2e(gk, shape, inputs, kb, vb, out, ws, stream, dev, K, W, units, dist):
+def run_e2e(gk, shape, inputs, kv, out, ws, stream, dev, K, W, units, dist):
     """Time K steps fed from pinned host memory: per step one H2D copy of all
     inputs (packed), append + attention, one D2H copy of the output.  Returns
     (max ms over ranks, units over ranks, H2D bytes/step, D2H bytes/step)."""
@@ -257,8 +265,8 @@ def run_e2e(gk, shape, inputs, kb, vb, out, ws, stream, dev, K, W, units, dist):
         if k >= 2:
             stream.wait_event(ev_out[i])         # output i of step k-2 has been read back
         gk.gk_kv_append(shape, d["k_new"], d["v_new"], d["cos"], d["sin"], d["k_scale"],
-                        d["v_scale"], d["upd_full"], d["upd_swa"], d["active"], kb, vb, stream=sh)
-        gk.gk_decode_attn_stack(shape, d["q"], kb, vb, d["k_scale"], d["v_scale"], d["cos"],
+                        d["v_scale"], d["upd_full"], d["upd_swa"], d["active"], kv, stream=sh)
+        gk.gk_decode_attn_stack(shape, d["q"], kv, d["k_scale"], d["v_scale"], d["cos"],
                                 d["sin"], d["bt_full"], d["bt_swa"], d["pos"], d["pos_w"],
                                 d["active"], outs[i], None, ws, stream=sh)
         ev_done[i].record(stream)
@@ -304,7 +312,19 @@ def run_gk(args):
                upd_full=t(c.upd_full, torch.int32), upd_swa=t(c.upd_swa, torch.int32),
                active=t(c.active, torch.uint8))
     q, k_new, v_new = st["q"].contiguous(), st["k_new"].contiguous(), st["v_new"].contiguous()
-    kb, vb = gk.split_group_buffers(cache)
+    k_layout = gk.GK_K_PLAIN if args.k_layout == "plain" else gk.GK_K_PACKED
+    if args.kv_form == "stacked":
+        # K_cache / V_cache with a leading group axis, one allocation each
+        kst = torch.stack([b[0] for b in cache])
+        vst = torch.stack([b[1] for b in cache])
+        cache = [(kst[j], vst[j]) for j in range(len(cache))]  # the same bytes, per group
+        kc = kst
+        if k_layout == gk.GK_K_PACKED:
+            G, nbk, kvh, Bk, Dk = kst.shape
+            kc = kst.view(G, nbk, kvh, Bk // 2, Dk, 2)
+        kv = gk.kv_stacked(kc, vst)
+    else:
+        kv = gk.kv_from_group_buffers(cache, k_layout)
     out = torch.empty(w.num_layers, w.batch, w.num_q_heads, w.head_dim, dtype=torch.bfloat16,
                       device=dev)
     if args.ws_min:   # smallest workspace: no split-KV (profiling the unsplit stage loop)
@@ -316,18 +336,18 @@ def run_gk(args):
 
     def append():
         gk.gk_kv_append(shape, k_new, v_new, ctl["cos"], ctl["sin"], ctl["k_scale"],
-                        ctl["v_scale"], ctl["upd_full"], ctl["upd_swa"], ctl["active"], kb, vb,
+                        ctl["v_scale"], ctl["upd_full"], ctl["upd_swa"], ctl["active"], kv,
                         stream=sh)
 
     def attention():
-        gk.gk_decode_attn_stack(shape, q, kb, vb, ctl["k_scale"], ctl["v_scale"], ctl["cos"],
+        gk.gk_decode_attn_stack(shape, q, kv, ctl["k_scale"], ctl["v_scale"], ctl["cos"],
                                 ctl["sin"], ctl["bt_full"], ctl["bt_swa"], ctl["pos"],
                                 ctl["pos_w"], ctl["active"], out, None, ws, stream=sh)
 
     def fused_step():
         gk.gk_decode_step(shape, q, k_new, v_new, ctl["cos"], ctl["sin"], ctl["k_scale"],
                           ctl["v_scale"], ctl["upd_full"], ctl["upd_swa"], ctl["bt_full"],
-                          ctl["bt_swa"], ctl["pos"], ctl["pos_w"], ctl["active"], kb, vb, out,
+                          ctl["bt_swa"], ctl["pos"], ctl["pos_w"], ctl["active"], kv, out,
                           None, ws, stream=sh)
 
     if args.step == "fused":
@@ -393,7 +413,7 @@ def run_gk(args):
     # copy streams so that step k+1's upload and step k's download overlap
     # step k's kernels.
     e2e_ms, e2e_units, h2d, d2h = run_e2e(gk, shape, dict(q=q, k_new=k_new, v_new=v_new, **ctl),
-                                          kb, vb, out, ws, stream, dev, K, W, units, dist)
+                                          kv, out, ws, stream, dev, K, W, units, dist)
     if gk.gk_read_device_error() != 0:
         raise RuntimeError("device error word set during the timed region")
 
@@ -411,7 +431,8 @@ def run_gk(args):
         "precision": "KV E4M3 codes; q/out bf16; QK^T and PV on f16 tensor-core MMA with fp32 "
                      "accumulation; fp32 online softmax",
         "data": "synthetic (seeded gk_inputs workload)",
-        "config": workload_config(w, c, f"inputs larger than L2: {kv_bytes / 1e9:.2f} GB KV read per step"),
+        "config": workload_config(w, c, f"inputs larger than L2: {kv_bytes / 1e9:.2f} GB KV read per step",
+                                  kv_layout_desc(args.k_layout, args.kv_form)),
         "impl": "gk",
         "attn_ms": round(attn_ms, 4),
         "append_ms": round(append_ms, 4),
@@ -431,7 +452,8 @@ def run_gk(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = {k: gi.bf16_bits(v) for k, v in st.items()}
-        v_cpu, n_done, secs, used = oracle_sample(w, c, host, cache, args.cpu_budget)
+        v_cpu, n_done, secs, used = oracle_sample(w, c, host, cache, args.cpu_budget,
+                                                  k_layout=k_layout)
         line["cpu_baseline"] = {
             "value": round(v_cpu, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{len(used)} rows x {w.num_layers} layers (all kv heads), oracle append + "
@@ -476,7 +498,7 @@ def run_reference(args):
             if (b, j) not in pools:
                 ids = np.concatenate([np.asarray(c.full_blocks[b], np.int64),
                                       np.asarray(c.swa_blocks[b], np.int64)])
-                idx = torch.as_tensor(ids, device=cache[j].device)
+                idx = torch.as_tensor(ids, device=cache[j][0].device)
                 pools[(b, j)] = (cache[j][0].index_select(0, idx).cpu().numpy().reshape(-1),
                                  cache[j][1].index_select(0, idx).cpu().numpy().reshape(-1))
     for s in range(args.warmup):
@@ -514,6 +536,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--step", choices=["split", "fused"], default="split",
                     help="split: gk_kv_append + gk_decode_attn_stack; fused: gk_decode_step")
+    ap.add_argument("--k-layout", choices=["packed", "plain"], default="packed",
+                    help="K through the packed view (the page's layout) or unpacked like V")
+    ap.add_argument("--kv-form", choices=["per_group", "stacked"], default="per_group",
+                    help="per-group K/V buffers or stacked K_cache/V_cache")
     ap.add_argument("--ws-min", action="store_true",
                     help="use the minimum attention workspace (no split-KV chunks)")
     args = ap.parse_args(argv)

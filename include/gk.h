@@ -11,8 +11,11 @@
  *     positions, two KV-update indices) are shared by all layers;
  *   - section "KV-cache layout (per-buffer, HMA-preserving)": one base-0 group
  *     buffer [2, num_blocks, kv, block, d] per layer pair, K half then V half;
- *     K is read through the packed FP8 view [.., block/2, d, 2], V is never
- *     packed.
+ *     K is read through the packed FP8 view [.., block/2, d, 2] (or unpacked,
+ *     like V), V is never packed;
+ *   - section "Kernel contract": the cache is passed either as per-group K and
+ *     V buffers or as stacked K_cache / V_cache, exactly one of the two forms
+ *     (gk_kv_cache below).
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers unless a parameter says "host".
@@ -42,11 +45,13 @@
  *   pos, pos_w        int32 [Bt]                  absolute / window-frame position of the new token
  *   upd_full, upd_swa int32 [Bt]                  flat slot = block * B + offset
  *   active            uint8 [Bt]                  0 = row skipped (no write, zero output)
- *   k_bufs[j], v_bufs[j]  HOST arrays of NL/2 DEVICE pointers: the K and V halves of
- *                     group buffer j, each num_blocks * Hkv * B * D bytes, 16-byte aligned.
+ *   kv                the cache (gk_kv_cache): group buffer j's K and V halves, each
+ *                     num_blocks * Hkv * B * D bytes (one FP8 byte per element):
  *                     K byte (pb, h, t, e) = ((pb*Hkv + h)*(B/2) + t/2)*(2D) + 2e + (t & 1)
+ *                                            (GK_K_PACKED, the view [.., B/2, D, 2])
+ *                                          = ((pb*Hkv + h)*B + t)*D + e   (GK_K_PLAIN)
  *                     V byte (pb, h, t, e) = ((pb*Hkv + h)*B + t)*D + e
- * Supported shapes (version 1): D == 64, G == 8, B == 16 or a multiple of 32 up to 1024,
+ * Supported shapes: D == 64, G == 8, B == 16 or a multiple of 32 up to 1024,
  * NL even and <= 128, Bt <= 8192.  Other shapes return GK_ERR_UNSUPPORTED.
  */
 #ifndef GK_H
@@ -76,6 +81,33 @@ typedef enum {
 #define GK_DEVERR_TIMEOUT 0x8u  /* a shared-memory barrier wait hit its iteration limit */
 #define GK_DEVERR_PLAN 0x10u    /* the work plan did not fit the workspace */
 
+/* K layouts.  The page infers packed-ness from the K tensor's rank
+ * (k.dim() == v.dim() + 1); across this ABI it is stated. */
+#define GK_K_PACKED 0 /* K through the packed view [.., B/2, D, 2]: tokens 2p, 2p+1 interleaved */
+#define GK_K_PLAIN 1  /* K laid out like V: [.., B, D] */
+
+/*
+ * gk_kv_cache -- the KV cache in one of the page's two forms ("GPT-OSS-120B
+ * giga-kernel decode", section "Kernel contract": the kernel takes per-group
+ * buffers or the stacked K_cache / V_cache and asserts that exactly one form
+ * is present).  Set the pointers of exactly one form and leave the other form's
+ * NULL; anything else is GK_ERR_INVALID_ARG.
+ *   per-group: k_bufs[j], v_bufs[j] (HOST arrays of NL/2 DEVICE pointers) are
+ *              the K and V halves of group buffer j, each 16-byte aligned;
+ *   stacked:   k_cache, v_cache (DEVICE pointers, 16-byte aligned) hold the
+ *              NL/2 halves back to back, [NL/2, num_blocks, Hkv, B, D] bytes:
+ *              group j's K half starts at k_cache + j * num_blocks*Hkv*B*D.
+ * Offsets are 64-bit throughout, so a stacked cache may exceed 4 GiB.
+ * The library reads the pointer arrays during the call only.
+ */
+typedef struct {
+    void *const *k_bufs;
+    void *const *v_bufs;
+    void *k_cache;
+    void *v_cache;
+    int32_t k_layout; /* GK_K_PACKED or GK_K_PLAIN */
+} gk_kv_cache;
+
 typedef struct {
     int32_t num_layers;      /* NL, even: layer pairs (2j, 2j+1) share group buffer j */
     int32_t batch;           /* Bt */
@@ -98,17 +130,17 @@ typedef struct {
  *   slot = (i even) ? upd_swa[b] : upd_full[b];  pb = slot / B;  t = slot % B
  *   k' = RoPE(k_new[i,b,h,:], cos[b], sin[b]) in IEEE fp32, no fused multiply-add:
  *        k'_e = k_e*c_e - k_{e+D/2}*s_e,  k'_{e+D/2} = k_{e+D/2}*c_e + k_e*s_e
- *   K_{i/2}[packed (pb,h,t,e)] = E4M3(k'_e / k_scale[i])       (fp32 division, RNE)
- *   V_{i/2}[plain  (pb,h,t,e)] = E4M3(v_new[i,b,h,e] / v_scale[i])
+ *   K_{i/2}[(pb,h,t,e)] = E4M3(k'_e / k_scale[i])   (fp32 division, RNE; kv->k_layout)
+ *   V_{i/2}[(pb,h,t,e)] = E4M3(v_new[i,b,h,e] / v_scale[i])
  * E4M3 = round to nearest, ties to even mantissa, saturating to +-448; NaN -> 0x7F.
  * Inactive rows write nothing.  No other byte of any buffer changes.
- * Returns GK_ERR_INVALID_ARG for null pointers or inconsistent shapes.
+ * Returns GK_ERR_INVALID_ARG for null pointers, inconsistent shapes or a kv
+ * that does not hold exactly one form.
  */
 gk_status gk_kv_append(const gk_shape *shape, const void *k_new, const void *v_new,
                        const float *cos, const float *sin, const float *k_scale,
                        const float *v_scale, const int32_t *upd_full, const int32_t *upd_swa,
-                       const uint8_t *active, void *const *k_bufs, void *const *v_bufs,
-                       void *stream);
+                       const uint8_t *active, const gk_kv_cache *kv, void *stream);
 
 /*
  * gk_attn_workspace_bytes -- recommended workspace size for gk_decode_attn_stack.
@@ -137,10 +169,11 @@ size_t gk_attn_workspace_min_bytes(const gk_shape *shape);
  * it is overwritten by every call (do not share one workspace between calls
  * that may overlap on the device).
  * Returns GK_ERR_WORKSPACE for a missing/small/misaligned workspace,
- * GK_ERR_INVALID_ARG for null or non-16-byte-aligned tensors.
+ * GK_ERR_INVALID_ARG for null or non-16-byte-aligned tensors or a kv that does
+ * not hold exactly one form.
  */
-gk_status gk_decode_attn_stack(const gk_shape *shape, const void *q, void *const *k_bufs,
-                               void *const *v_bufs, const float *k_scale, const float *v_scale,
+gk_status gk_decode_attn_stack(const gk_shape *shape, const void *q, const gk_kv_cache *kv,
+                               const float *k_scale, const float *v_scale,
                                const float *cos, const float *sin, const int32_t *bt_full,
                                const int32_t *bt_swa, const int32_t *pos, const int32_t *pos_w,
                                const uint8_t *active, void *out, float *out_f32,
@@ -167,7 +200,7 @@ gk_status gk_decode_step(const gk_shape *shape, const void *q, const void *k_new
                          const float *k_scale, const float *v_scale, const int32_t *upd_full,
                          const int32_t *upd_swa, const int32_t *bt_full, const int32_t *bt_swa,
                          const int32_t *pos, const int32_t *pos_w, const uint8_t *active,
-                         void *const *k_bufs, void *const *v_bufs, void *out, float *out_f32,
+                         const gk_kv_cache *kv, void *out, float *out_f32,
                          void *workspace, size_t ws_bytes, void *stream);
 
 /*
@@ -195,8 +228,8 @@ gk_status gk_decode_step(const gk_shape *shape, const void *q, const void *k_new
  *     array and give wrong results: order them.
  */
 #define GK_STATIC_SCRATCH_BYTES (16u << 20)
-gk_status gk_decode_attn_stack_static(const gk_shape *shape, const void *q, void *const *k_bufs,
-                                      void *const *v_bufs, const float *k_scale,
+gk_status gk_decode_attn_stack_static(const gk_shape *shape, const void *q,
+                                      const gk_kv_cache *kv, const float *k_scale,
                                       const float *v_scale, const float *cos, const float *sin,
                                       const int32_t *bt_full, const int32_t *bt_swa,
                                       const int32_t *pos, const int32_t *pos_w,
@@ -244,7 +277,7 @@ gk_status gk_kv_budget(uint64_t total_bytes, uint64_t used_bytes, double gpu_mem
 /* Human-readable name of a status code (static string). */
 const char *gk_status_str(gk_status status);
 
-/* Library ABI version (1). */
+/* Library ABI version (2: the cache is passed as a gk_kv_cache). */
 int32_t gk_abi_version(void);
 
 #ifdef __cplusplus

@@ -44,9 +44,10 @@ def build(force: bool = False) -> str:
 
 
 class Shape(ctypes.Structure):
+    """ora_shape; k_layout 0 = packed K view, 1 = unpacked K (laid out like V)."""
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_layers", "batch", "num_q_heads", "num_kv_heads", "head_dim",
-        "block_size", "num_blocks", "window", "max_blocks_full", "max_blocks_swa")]
+        "block_size", "num_blocks", "window", "max_blocks_full", "max_blocks_swa", "k_layout")]
 
 
 def _p(a):
@@ -155,8 +156,9 @@ def make_shape(**kw) -> Shape:
 
 def kv_append(shape: Shape, k_new, v_new, cos, sin, k_scale, v_scale, upd_full, upd_swa,
               active, k_bufs, v_bufs) -> int:
-    """Quantise and write the new token's K (packed) and V (plain) into the
-    group buffers, in place.  k_new/v_new are bf16 bit patterns (uint16)."""
+    """Quantise and write the new token's K (packed, or unpacked when
+    shape.k_layout == 1) and V (plain) into the group buffers, in place.
+    k_new/v_new are bf16 bit patterns (uint16)."""
     k_new = _c(k_new, np.uint16)
     v_new = _c(v_new, np.uint16)
     cos = _c(cos, np.float32)

@@ -19,6 +19,9 @@
  *       2p and 2p+1 of one channel, so K byte (pb, h, t, e) sits at
  *       ((pb*Hkv + h)*(B/2) + t/2)*(2D) + 2e + (t & 1).  V is never packed:
  *       ((pb*Hkv + h)*B + t)*D + e.                          [GK KV-cache layout]
+ *       Unpacked K (k_layout = 1) is the tensor the packed view is taken on,
+ *       [.., block, d] like V: ((pb*Hkv + h)*B + t)*D + e.  [GK KV-cache layout,
+ *       Kernel contract: packed-ness read from the K rank]
  *   R2  RoPE: rotate-half pairs (e, e + D/2) with the per-sequence cos/sin rows
  *       given as inputs [Bt, D/2].                            [GK Kernel contract]
  *   R3  Quantisation: code = E4M3_rne_satfinite(x / scale), one k and one v scale
@@ -46,6 +49,7 @@
 typedef struct {
     int32_t num_layers, batch, num_q_heads, num_kv_heads, head_dim;
     int32_t block_size, num_blocks, window, max_blocks_full, max_blocks_swa;
+    int32_t k_layout; /* 0: packed K view, 1: unpacked K (laid out like V) */
 } ora_shape;
 
 /* ------------------------------------------------------------------------- */
@@ -160,6 +164,14 @@ int64_t ora_v_offset(int32_t Hkv, int32_t B, int32_t D, int64_t pb, int32_t h, i
     return ((pb * Hkv + h) * (int64_t)B + t) * (int64_t)D + e;
 }
 
+/* Byte of K element (pb, h, t, e) in the shape's K layout. */
+static int64_t k_byte(const ora_shape *sh, int64_t pb, int32_t h, int32_t t, int32_t e)
+{
+    if (sh->k_layout == 0)
+        return ora_k_offset(sh->num_kv_heads, sh->block_size, sh->head_dim, pb, h, t, e);
+    return ora_v_offset(sh->num_kv_heads, sh->block_size, sh->head_dim, pb, h, t, e);
+}
+
 /* Per-layer resources by parity [GK Kernel contract], reading R7. */
 static int layer_is_swa(int32_t i) { return (i % 2) == 0; }
 
@@ -233,7 +245,7 @@ int ora_kv_append(const ora_shape *sh, const uint16_t *k_new, const uint16_t *v_
                 for (int32_t e = 0; e < D; ++e) {
                     float kq = kr[e] / k_scale[i];
                     float vq = bf16_to_f32(vr16[e]) / v_scale[i];
-                    k_bufs[j][ora_k_offset(Hkv, B, D, pb, h, t, e)] = ora_e4m3_encode(kq);
+                    k_bufs[j][k_byte(sh, pb, h, t, e)] = ora_e4m3_encode(kq);
                     v_bufs[j][ora_v_offset(Hkv, B, D, pb, h, t, e)] = ora_e4m3_encode(vq);
                 }
             }
@@ -309,7 +321,7 @@ static int load_kv(const ora_shape *sh, const ora_attn_inputs *in, int32_t i, in
     if (pb < 0 || pb >= sh->num_blocks)
         return -1;
     for (int32_t e = 0; e < D; ++e) {
-        k[e] = ora_e4m3_decode(in->kbuf[ora_k_offset(Hkv, B, D, pb, kvh, off, e)]) * (double)in->k_scale[i];
+        k[e] = ora_e4m3_decode(in->kbuf[k_byte(sh, pb, kvh, off, e)]) * (double)in->k_scale[i];
         v[e] = ora_e4m3_decode(in->vbuf[ora_v_offset(Hkv, B, D, pb, kvh, off, e)]) * (double)in->v_scale[i];
     }
     return 0;

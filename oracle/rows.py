@@ -14,11 +14,12 @@ from . import attn_one, kv_append, make_shape
 
 
 def row_pair_from_pool(w, c, step_host: dict, kpool: np.ndarray, vpool: np.ndarray, j: int,
-                       b: int, kvhs=None) -> dict:
+                       b: int, kvhs=None, k_layout: int = 0) -> dict:
     """w, c: the workload and its control tensors (gk_inputs.Workload/Control).
     step_host: q, k_new, v_new as uint16 bf16 bit arrays.  kpool/vpool: bytes
     of row b's full blocks followed by its window blocks (K halves and V
     halves, each block Hkv*B*D bytes), from the cache before the append.
+    k_layout: 0 packed K view, 1 unpacked K.
     Returns {(layer, kvh): [G, D] float64} for layers 2j and 2j+1."""
     B, Hkv, D, NL = w.block_size, w.num_kv_heads, w.head_dim, w.num_layers
     kvhs = range(Hkv) if kvhs is None else kvhs
@@ -39,7 +40,7 @@ def row_pair_from_pool(w, c, step_host: dict, kpool: np.ndarray, vpool: np.ndarr
     upd_s = np.array([bt_swa[0, pos // B - b0] * B + pos % B], np.int32)
     sh = make_shape(num_layers=NL, batch=1, num_q_heads=w.num_q_heads, num_kv_heads=Hkv,
                     head_dim=D, block_size=B, num_blocks=pad + 1, window=w.window,
-                    max_blocks_full=mbf, max_blocks_swa=c.max_blocks_swa)
+                    max_blocks_full=mbf, max_blocks_swa=c.max_blocks_swa, k_layout=k_layout)
     # only group j's pool is real; the other groups get scratch pools
     scratch_k = [np.zeros(kmini.size, np.uint8) for _ in range(NL // 2)]
     scratch_v = [np.zeros(vmini.size, np.uint8) for _ in range(NL // 2)]

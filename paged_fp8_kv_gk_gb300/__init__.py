@@ -10,7 +10,10 @@ The functions carry the C names: ``gk_kv_append``, ``gk_decode_attn_stack``,
 ``gk_attn_workspace_bytes``, ``gk_attn_workspace_min_bytes``,
 ``gk_e4m3_quantize``, ``gk_kv_budget``, ``gk_read_device_error``, ``gk_status_str``,
 ``gk_abi_version``.  Tensors are torch tensors; the stream defaults to torch's
-current stream on the tensors' device.
+current stream on the tensors' device.  The cache is a ``KvCache``: per-group
+K and V buffers or stacked ``K_cache`` / ``V_cache``, exactly one of the two,
+with packed-ness read from the K tensors' rank as the "GPT-OSS-120B giga-kernel
+decode" page describes (section "KV-cache layout": ``k.dim() == v.dim() + 1``).
 """
 from __future__ import annotations
 
@@ -26,6 +29,7 @@ GK_OK, GK_ERR_INVALID_ARG, GK_ERR_UNSUPPORTED, GK_ERR_WORKSPACE, GK_ERR_CUDA, \
     GK_ERR_DEVICE_BOUNDS, GK_ERR_BUDGET = range(7)
 GK_DEVERR_SLOT, GK_DEVERR_BLOCK, GK_DEVERR_POS, GK_DEVERR_TIMEOUT, GK_DEVERR_PLAN = \
     0x1, 0x2, 0x4, 0x8, 0x10
+GK_K_PACKED, GK_K_PLAIN = 0, 1
 
 HEADER = os.path.join(_build.INCLUDE, "gk.h")
 
@@ -48,6 +52,122 @@ class Shape(ctypes.Structure):
     @classmethod
     def make(cls, **kw) -> "Shape":
         return cls(**{k: int(v) for k, v in kw.items()})
+
+
+class KvCacheC(ctypes.Structure):
+    """gk_kv_cache."""
+    _fields_ = [("k_bufs", ctypes.c_void_p), ("v_bufs", ctypes.c_void_p),
+                ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+                ("k_layout", ctypes.c_int32)]
+
+
+class KvCache:
+    """The KV cache in one of its two forms ("Kernel contract": per-group
+    buffers or stacked K_cache / V_cache, exactly one present).
+
+    per-group: ``k_bufs[j]``, ``v_bufs[j]`` are group buffer j's K and V halves:
+      V ``[num_blocks, kv, block, d]`` uint8, K the same (unpacked) or the packed
+      view ``[num_blocks, kv, block // 2, d, 2]``;
+    stacked: ``k_cache``, ``v_cache`` with a leading group axis (``[G, ...]``).
+    ``k_layout`` is read from the ranks (``k.dim() == v.dim() + 1`` means packed);
+    it must be given only when the buffers are raw device addresses (ints).
+    Holds references to the tensors and the pointer arrays it hands the library.
+    """
+
+    def __init__(self, k_bufs=None, v_bufs=None, k_cache=None, v_cache=None,
+                 k_layout: Optional[int] = None):
+        per_group = k_bufs is not None or v_bufs is not None
+        stacked = k_cache is not None or v_cache is not None
+        if per_group == stacked:
+            raise ValueError("pass exactly one KV form: (k_bufs, v_bufs) or (k_cache, v_cache)")
+        if per_group and (k_bufs is None or v_bufs is None or len(k_bufs) != len(v_bufs)):
+            raise ValueError("k_bufs and v_bufs must both be given, one per group buffer")
+        if stacked and (k_cache is None or v_cache is None):
+            raise ValueError("k_cache and v_cache must both be given")
+        ks = list(k_bufs) if per_group else [k_cache]
+        vs = list(v_bufs) if per_group else [v_cache]
+        tensors = [(k, v) for k, v in zip(ks, vs) if not isinstance(k, int)
+                   and not isinstance(v, int)]
+        if tensors:
+            inferred = {infer_k_layout(k, v) for k, v in tensors}
+            if len(inferred) != 1:
+                raise ValueError("all group buffers must have one K layout")
+            inferred = inferred.pop()
+            if k_layout is not None and k_layout != inferred:
+                raise ValueError("k_layout disagrees with the K tensors' rank")
+            k_layout = inferred
+        elif k_layout is None:
+            raise ValueError("k_layout is required for raw device addresses")
+        if k_layout not in (GK_K_PACKED, GK_K_PLAIN):
+            raise ValueError(f"k_layout {k_layout}")
+        self.per_group = per_group
+        self.k_layout = int(k_layout)
+        self._keep = (ks, vs)
+        c = KvCacheC(k_layout=self.k_layout)
+        if per_group:
+            self._k_arr = _ptr_array(ks, "k_bufs")
+            self._v_arr = _ptr_array(vs, "v_bufs")
+            c.k_bufs = ctypes.cast(self._k_arr, ctypes.c_void_p)
+            c.v_bufs = ctypes.cast(self._v_arr, ctypes.c_void_p)
+        else:
+            c.k_cache = _ptr(k_cache, None, "k_cache")
+            c.v_cache = _ptr(v_cache, None, "v_cache")
+        self.c = c
+
+    def check(self, shape) -> None:
+        """Buffer sizes against the shape (the C ABI cannot see them)."""
+        sh = _as_shape(shape)
+        groups = sh.num_layers // 2
+        half = sh.num_blocks * sh.num_kv_heads * sh.block_size * sh.head_dim
+        ks, vs = self._keep
+        if self.per_group and len(ks) < groups:
+            raise ValueError(f"{len(ks)} group buffers for {sh.num_layers} layers")
+        want = half if self.per_group else groups * half
+        for t in ks + vs:
+            if not isinstance(t, int) and t.numel() * t.element_size() < want:
+                raise ValueError(f"a cache buffer holds {t.numel() * t.element_size()} bytes, "
+                                 f"the shape needs {want}")
+
+    def param(self):
+        return ctypes.byref(self.c)
+
+
+def infer_k_layout(k, v) -> int:
+    """Packed-ness from the ranks, as the page's bind step infers it
+    (``k.dim() == v.dim() + 1``: the packed view's extra trailing axis of 2)."""
+    kd, vd = k.dim(), v.dim()
+    if kd == vd + 1 and k.shape[-1] == 2:
+        return GK_K_PACKED
+    if kd == vd:
+        return GK_K_PLAIN
+    raise ValueError(f"K shape {tuple(k.shape)} vs V shape {tuple(v.shape)}: "
+                     "neither the packed view nor the plain layout")
+
+
+def kv_from_group_buffers(bufs: Sequence, k_layout: int = GK_K_PACKED) -> KvCache:
+    """Group buffers [2, num_blocks, kv, block, d] (K half, then V half) -> the
+    per-group KvCache, K viewed packed ([.., block // 2, d, 2]) or plain."""
+    ks = []
+    for b in bufs:
+        k = b[0]
+        if k_layout == GK_K_PACKED:
+            nb, kv, B, D = k.shape
+            k = k.view(nb, kv, B // 2, D, 2)
+        ks.append(k)
+    return KvCache(k_bufs=ks, v_bufs=[b[1] for b in bufs])
+
+
+def kv_stacked(k_cache, v_cache) -> KvCache:
+    """Stacked K_cache / V_cache ([G, num_blocks, kv, block, d], K optionally
+    as the packed view [G, num_blocks, kv, block // 2, d, 2])."""
+    return KvCache(k_cache=k_cache, v_cache=v_cache)
+
+
+def _kv(kv, shape) -> "ctypes._CArgObject":
+    if not isinstance(kv, KvCache):
+        raise TypeError("kv must be a KvCache (kv_from_group_buffers, kv_stacked)")
+    kv.check(shape)
+    return kv.param()
 
 
 def declared_functions() -> list:
@@ -73,17 +193,17 @@ def lib(build_if_needed: bool = True) -> ctypes.CDLL:
             L.gk_abi_version.restype = i32
             L.gk_abi_version.argtypes = []
             L.gk_kv_append.restype = ctypes.c_int
-            L.gk_kv_append.argtypes = [sp] + [vp] * 12
+            L.gk_kv_append.argtypes = [sp] + [vp] * 11
             L.gk_attn_workspace_bytes.restype = sz
             L.gk_attn_workspace_bytes.argtypes = [sp, vp]
             L.gk_attn_workspace_min_bytes.restype = sz
             L.gk_attn_workspace_min_bytes.argtypes = [sp]
             L.gk_decode_attn_stack.restype = ctypes.c_int
-            L.gk_decode_attn_stack.argtypes = [sp] + [vp] * 15 + [sz, vp]
+            L.gk_decode_attn_stack.argtypes = [sp] + [vp] * 14 + [sz, vp]
             L.gk_decode_step.restype = ctypes.c_int
-            L.gk_decode_step.argtypes = [sp] + [vp] * 19 + [sz, vp]
+            L.gk_decode_step.argtypes = [sp] + [vp] * 18 + [sz, vp]
             L.gk_decode_attn_stack_static.restype = ctypes.c_int
-            L.gk_decode_attn_stack_static.argtypes = [sp] + [vp] * 15
+            L.gk_decode_attn_stack_static.argtypes = [sp] + [vp] * 14
             L.gk_e4m3_quantize.restype = ctypes.c_int
             L.gk_e4m3_quantize.argtypes = [vp, ctypes.c_float, vp, i64, vp]
             L.gk_kv_budget.restype = ctypes.c_int
@@ -161,7 +281,7 @@ def gk_attn_workspace_min_bytes(shape) -> int:
 
 
 def gk_kv_append(shape, k_new, v_new, cos, sin, k_scale, v_scale, upd_full, upd_swa, active,
-                 k_bufs, v_bufs, stream=None) -> None:
+                 kv: KvCache, stream=None) -> None:
     import torch
     sh = _as_shape(shape)
     st = lib().gk_kv_append(
@@ -169,13 +289,11 @@ def gk_kv_append(shape, k_new, v_new, cos, sin, k_scale, v_scale, upd_full, upd_
         _ptr(cos, torch.float32, "cos"), _ptr(sin, torch.float32, "sin"),
         _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
         _ptr(upd_full, torch.int32, "upd_full"), _ptr(upd_swa, torch.int32, "upd_swa"),
-        _ptr(active, torch.uint8, "active"),
-        ctypes.cast(_ptr_array(k_bufs, "k_bufs"), ctypes.c_void_p),
-        ctypes.cast(_ptr_array(v_bufs, "v_bufs"), ctypes.c_void_p), _stream(stream, k_new))
+        _ptr(active, torch.uint8, "active"), _kv(kv, sh), _stream(stream, k_new))
     _check(st, "gk_kv_append")
 
 
-def gk_decode_attn_stack(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, bt_full, bt_swa,
+def gk_decode_attn_stack(shape, q, kv: KvCache, k_scale, v_scale, cos, sin, bt_full, bt_swa,
                          pos, pos_w, active, out, out_f32=None, workspace=None,
                          stream=None) -> None:
     import torch
@@ -183,9 +301,7 @@ def gk_decode_attn_stack(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, b
     if workspace is None:
         raise ValueError("workspace is required (size: gk_attn_workspace_bytes(shape))")
     st = lib().gk_decode_attn_stack(
-        ctypes.byref(sh), _ptr(q, torch.bfloat16, "q"),
-        ctypes.cast(_ptr_array(k_bufs, "k_bufs"), ctypes.c_void_p),
-        ctypes.cast(_ptr_array(v_bufs, "v_bufs"), ctypes.c_void_p),
+        ctypes.byref(sh), _ptr(q, torch.bfloat16, "q"), _kv(kv, sh),
         _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
         _ptr(cos, torch.float32, "cos"), _ptr(sin, torch.float32, "sin"),
         _ptr(bt_full, torch.int32, "bt_full"), _ptr(bt_swa, torch.int32, "bt_swa"),
@@ -197,7 +313,7 @@ def gk_decode_attn_stack(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, b
 
 
 def gk_decode_step(shape, q, k_new, v_new, cos, sin, k_scale, v_scale, upd_full, upd_swa,
-                   bt_full, bt_swa, pos, pos_w, active, k_bufs, v_bufs, out, out_f32=None,
+                   bt_full, bt_swa, pos, pos_w, active, kv: KvCache, out, out_f32=None,
                    workspace=None, stream=None) -> None:
     """gk_kv_append + gk_decode_attn_stack in one attention launch."""
     import torch
@@ -211,15 +327,13 @@ def gk_decode_step(shape, q, k_new, v_new, cos, sin, k_scale, v_scale, upd_full,
         _ptr(v_scale, torch.float32, "v_scale"), _ptr(upd_full, torch.int32, "upd_full"),
         _ptr(upd_swa, torch.int32, "upd_swa"), _ptr(bt_full, torch.int32, "bt_full"),
         _ptr(bt_swa, torch.int32, "bt_swa"), _ptr(pos, torch.int32, "pos"),
-        _ptr(pos_w, torch.int32, "pos_w"), _ptr(active, torch.uint8, "active"),
-        ctypes.cast(_ptr_array(k_bufs, "k_bufs"), ctypes.c_void_p),
-        ctypes.cast(_ptr_array(v_bufs, "v_bufs"), ctypes.c_void_p),
+        _ptr(pos_w, torch.int32, "pos_w"), _ptr(active, torch.uint8, "active"), _kv(kv, sh),
         _ptr(out, torch.bfloat16, "out"), _ptr(out_f32, torch.float32, "out_f32", allow_none=True),
         _ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()), _stream(stream, q))
     _check(st, "gk_decode_step")
 
 
-def gk_decode_attn_stack_static(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, bt_full,
+def gk_decode_attn_stack_static(shape, q, kv: KvCache, k_scale, v_scale, cos, sin, bt_full,
                                 bt_swa, pos, pos_w, active, out, out_f32=None,
                                 stream=None) -> None:
     """gk_decode_attn_stack without a caller workspace, for callers that cannot
@@ -229,9 +343,7 @@ def gk_decode_attn_stack_static(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos,
     import torch
     sh = _as_shape(shape)
     st = lib().gk_decode_attn_stack_static(
-        ctypes.byref(sh), _ptr(q, torch.bfloat16, "q"),
-        ctypes.cast(_ptr_array(k_bufs, "k_bufs"), ctypes.c_void_p),
-        ctypes.cast(_ptr_array(v_bufs, "v_bufs"), ctypes.c_void_p),
+        ctypes.byref(sh), _ptr(q, torch.bfloat16, "q"), _kv(kv, sh),
         _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
         _ptr(cos, torch.float32, "cos"), _ptr(sin, torch.float32, "sin"),
         _ptr(bt_full, torch.int32, "bt_full"), _ptr(bt_swa, torch.int32, "bt_swa"),
@@ -283,11 +395,6 @@ def gk_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     if st not in (GK_OK, GK_ERR_DEVICE_BOUNDS):
         raise GkError(st, "gk_selftest_wait_timeout")
     return int(bits.value)
-
-
-def split_group_buffers(bufs: Sequence):
-    """Group buffers [2, nb, kv, B, D] -> (K halves, V halves) as the ABI takes them."""
-    return [b[0] for b in bufs], [b[1] for b in bufs]
 
 
 def new_workspace(shape, device="cuda"):

@@ -43,6 +43,40 @@ static int64_t recommended_cap(const gk_shape& s) {
   return a < b ? a : b;
 }
 
+// The cache descriptor -> per-group K and V base pointers.  Exactly one of
+// the two forms must be present ("Kernel contract": the kernel asserts it).
+static gk_status resolve_kv(const gk_shape& s, const gk_kv_cache* kv, uint8_t** kb, uint8_t** vb,
+                            int* k_packed) {
+  if (!kv) return GK_ERR_INVALID_ARG;
+  const bool per_group = kv->k_bufs != nullptr || kv->v_bufs != nullptr;
+  const bool stacked = kv->k_cache != nullptr || kv->v_cache != nullptr;
+  if (per_group == stacked) return GK_ERR_INVALID_ARG;
+  if (kv->k_layout != GK_K_PACKED && kv->k_layout != GK_K_PLAIN) return GK_ERR_INVALID_ARG;
+  const int groups = s.num_layers / 2;
+  if (per_group) {
+    if (!kv->k_bufs || !kv->v_bufs) return GK_ERR_INVALID_ARG;
+    for (int j = 0; j < groups; ++j) {
+      if (!kv->k_bufs[j] || !kv->v_bufs[j] || !aligned16(kv->k_bufs[j]) ||
+          !aligned16(kv->v_bufs[j]))
+        return GK_ERR_INVALID_ARG;
+      kb[j] = static_cast<uint8_t*>(kv->k_bufs[j]);
+      vb[j] = static_cast<uint8_t*>(kv->v_bufs[j]);
+    }
+  } else {
+    if (!kv->k_cache || !kv->v_cache || !aligned16(kv->k_cache) || !aligned16(kv->v_cache))
+      return GK_ERR_INVALID_ARG;
+    // one half of a group buffer: a multiple of 16 bytes (D = 64), so every
+    // group's base stays 16-byte aligned
+    const int64_t half = int64_t(s.num_blocks) * s.num_kv_heads * s.block_size * s.head_dim;
+    for (int j = 0; j < groups; ++j) {
+      kb[j] = static_cast<uint8_t*>(kv->k_cache) + int64_t(j) * half;
+      vb[j] = static_cast<uint8_t*>(kv->v_cache) + int64_t(j) * half;
+    }
+  }
+  *k_packed = kv->k_layout == GK_K_PACKED ? 1 : 0;
+  return GK_OK;
+}
+
 WsLayout ws_layout(const gk_shape& s, size_t ws_bytes) {
   WsLayout L;
   const int64_t planes = int64_t(s.num_layers / 2) * s.num_kv_heads;
@@ -104,28 +138,22 @@ const char* gk_status_str(gk_status st) {
   return "GK_ERR_UNKNOWN";
 }
 
-int32_t gk_abi_version(void) { return 1; }
+int32_t gk_abi_version(void) { return 2; }
 
 gk_status gk_kv_append(const gk_shape* shape, const void* k_new, const void* v_new,
                        const float* cos, const float* sin, const float* k_scale,
                        const float* v_scale, const int32_t* upd_full, const int32_t* upd_swa,
-                       const uint8_t* active, void* const* k_bufs, void* const* v_bufs,
-                       void* stream) {
-  const gk_status st = check_shape(shape);
+                       const uint8_t* active, const gk_kv_cache* kv, void* stream) {
+  gk_status st = check_shape(shape);
   if (st != GK_OK) return st;
   if (!k_new || !v_new || !cos || !sin || !k_scale || !v_scale || !upd_full || !upd_swa ||
-      !active || !k_bufs || !v_bufs)
+      !active)
     return GK_ERR_INVALID_ARG;
   if (!aligned16(k_new) || !aligned16(v_new)) return GK_ERR_INVALID_ARG;
   AppendParams p;
   memset(&p, 0, sizeof(p));
-  const int groups = shape->num_layers / 2;
-  for (int j = 0; j < groups; ++j) {
-    if (!k_bufs[j] || !v_bufs[j] || !aligned16(k_bufs[j]) || !aligned16(v_bufs[j]))
-      return GK_ERR_INVALID_ARG;
-    p.kb[j] = static_cast<uint8_t*>(k_bufs[j]);
-    p.vb[j] = static_cast<uint8_t*>(v_bufs[j]);
-  }
+  st = resolve_kv(*shape, kv, p.kb, p.vb, &p.k_packed);
+  if (st != GK_OK) return st;
   p.k_new = static_cast<const uint16_t*>(k_new);
   p.v_new = static_cast<const uint16_t*>(v_new);
   p.cosb = cos;
@@ -168,16 +196,16 @@ struct AppendInputs {
 
 // Validation and launch shared by gk_decode_attn_stack and gk_decode_step
 // (app != nullptr: the fused step, where the units append the new token).
-static gk_status decode_attention(const gk_shape* shape, const void* q, void* const* k_bufs,
-                                  void* const* v_bufs, const float* k_scale, const float* v_scale,
+static gk_status decode_attention(const gk_shape* shape, const void* q, const gk_kv_cache* kv,
+                                  const float* k_scale, const float* v_scale,
                                   const float* cos, const float* sin, const int32_t* bt_full,
                                   const int32_t* bt_swa, const int32_t* pos, const int32_t* pos_w,
                                   const uint8_t* active, void* out, float* out_f32,
                                   void* workspace, size_t ws_bytes, void* stream,
                                   const AppendInputs* app) {
-  const gk_status st = check_shape(shape);
+  gk_status st = check_shape(shape);
   if (st != GK_OK) return st;
-  if (!q || !k_bufs || !v_bufs || !k_scale || !v_scale || !cos || !sin || !bt_full || !bt_swa ||
+  if (!q || !k_scale || !v_scale || !cos || !sin || !bt_full || !bt_swa ||
       !pos || !pos_w || !active || !out)
     return GK_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(out) || (out_f32 && !aligned16(out_f32)) || !aligned16(cos) ||
@@ -193,12 +221,15 @@ static gk_status decode_attention(const gk_shape* shape, const void* q, void* co
 
   AttnParams p;
   memset(&p, 0, sizeof(p));
-  const int groups = shape->num_layers / 2;
-  for (int j = 0; j < groups; ++j) {
-    if (!k_bufs[j] || !v_bufs[j] || !aligned16(k_bufs[j]) || !aligned16(v_bufs[j]))
-      return GK_ERR_INVALID_ARG;
-    p.kb[j] = static_cast<const uint8_t*>(k_bufs[j]);
-    p.vb[j] = static_cast<const uint8_t*>(v_bufs[j]);
+  {
+    uint8_t* kb[kMaxGroups];
+    uint8_t* vb[kMaxGroups];
+    st = resolve_kv(*shape, kv, kb, vb, &p.k_packed);
+    if (st != GK_OK) return st;
+    for (int j = 0; j < shape->num_layers / 2; ++j) {
+      p.kb[j] = kb[j];
+      p.vb[j] = vb[j];
+    }
   }
   if (app) {
     p.fused = 1;
@@ -259,14 +290,14 @@ static gk_status decode_attention(const gk_shape* shape, const void* q, void* co
 
 extern "C" {
 
-gk_status gk_decode_attn_stack(const gk_shape* shape, const void* q, void* const* k_bufs,
-                               void* const* v_bufs, const float* k_scale, const float* v_scale,
+gk_status gk_decode_attn_stack(const gk_shape* shape, const void* q, const gk_kv_cache* kv,
+                               const float* k_scale, const float* v_scale,
                                const float* cos, const float* sin, const int32_t* bt_full,
                                const int32_t* bt_swa, const int32_t* pos, const int32_t* pos_w,
                                const uint8_t* active, void* out, float* out_f32, void* workspace,
                                size_t ws_bytes, void* stream) {
-  return decode_attention(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, bt_full, bt_swa,
-                          pos, pos_w, active, out, out_f32, workspace, ws_bytes, stream, nullptr);
+  return decode_attention(shape, q, kv, k_scale, v_scale, cos, sin, bt_full, bt_swa, pos, pos_w,
+                          active, out, out_f32, workspace, ws_bytes, stream, nullptr);
 }
 
 gk_status gk_decode_step(const gk_shape* shape, const void* q, const void* k_new,
@@ -274,11 +305,11 @@ gk_status gk_decode_step(const gk_shape* shape, const void* q, const void* k_new
                          const float* k_scale, const float* v_scale, const int32_t* upd_full,
                          const int32_t* upd_swa, const int32_t* bt_full, const int32_t* bt_swa,
                          const int32_t* pos, const int32_t* pos_w, const uint8_t* active,
-                         void* const* k_bufs, void* const* v_bufs, void* out, float* out_f32,
+                         const gk_kv_cache* kv, void* out, float* out_f32,
                          void* workspace, size_t ws_bytes, void* stream) {
   const AppendInputs app = {k_new, v_new, upd_full, upd_swa};
-  return decode_attention(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, bt_full, bt_swa,
-                          pos, pos_w, active, out, out_f32, workspace, ws_bytes, stream, &app);
+  return decode_attention(shape, q, kv, k_scale, v_scale, cos, sin, bt_full, bt_swa, pos, pos_w,
+                          active, out, out_f32, workspace, ws_bytes, stream, &app);
 }
 
 gk_status gk_kv_budget(uint64_t total_bytes, uint64_t used_bytes, double gmu, double cap_fraction,

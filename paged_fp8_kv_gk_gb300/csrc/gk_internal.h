@@ -54,6 +54,7 @@ struct AppendParams {
   const uint8_t* active;
   uint8_t* kb[kMaxGroups];
   uint8_t* vb[kMaxGroups];
+  int k_packed;  // 1: K through the packed view, 0: K laid out like V
   int NL, Bt, Hkv, B, nb;
 };
 
@@ -97,6 +98,7 @@ struct AttnParams {
   const int32_t* upd_full;
   const int32_t* upd_swa;
   int fused;
+  int k_packed;  // 1: K through the packed view, 0: K laid out like V
   int NL, Bt, Hq, Hkv, B, nb, W, MBF, MBS;
 };
 

@@ -51,43 +51,6 @@ __device__ __forceinline__ float div_scale(float x, float s, float r) {
 // per group rather than a chain of dependent ones).
 constexpr int kAppendHeads = 8;
 
-// The append of one (layer, row, kv head) by one warp, the same arithmetic as
-// kv_append_kernel: lane l rotates the pair (l, l + 32) of k and converts
-// channels 2l, 2l + 1 of v.  Returns false (and sets the error bit) when the
-// update slot lies outside the buffer.
-__device__ __forceinline__ bool append_one(const uint16_t* k_new, const uint16_t* v_new,
-                                           const float* cosb, const float* sinb,
-                                           const float* k_scale, const float* v_scale,
-                                           const int32_t* upd_full, const int32_t* upd_swa,
-                                           uint8_t* kbuf, uint8_t* vbuf, int Bt, int Hkv, int B,
-                                           int nb, int i, int b, int h, int lane) {
-  const int32_t slot = (i & 1) ? upd_full[b] : upd_swa[b];
-  if (slot < 0 || int64_t(slot) >= int64_t(nb) * B) {
-    if (lane == 0) set_error(GK_DEVERR_SLOT);
-    return false;
-  }
-  const int64_t pb = slot / B;
-  const int t = slot % B;
-  const int64_t row = (int64_t(i) * Bt + b) * Hkv + h;
-  const float x = __uint_as_float(uint32_t(k_new[row * kHeadDim + lane]) << 16);
-  const float y = __uint_as_float(uint32_t(k_new[row * kHeadDim + lane + 32]) << 16);
-  const uint32_t vw = reinterpret_cast<const uint32_t*>(v_new + row * kHeadDim)[lane];
-  const float c = cosb[b * (kHeadDim / 2) + lane];
-  const float s = sinb[b * (kHeadDim / 2) + lane];
-  const float ks = k_scale[i], vs = v_scale[i];
-  const float kr_inv = exact_reciprocal(ks), vr_inv = exact_reciprocal(vs);
-  const float xr = __fsub_rn(__fmul_rn(x, c), __fmul_rn(y, s));
-  const float yr = __fadd_rn(__fmul_rn(y, c), __fmul_rn(x, s));
-  const uint32_t kc = f32x2_to_e4m3x2(div_scale(xr, ks, kr_inv), div_scale(yr, ks, kr_inv));
-  uint8_t* kdst = kbuf + ((pb * Hkv + h) * (B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1);
-  kdst[2 * lane] = uint8_t(kc & 0xffu);
-  kdst[2 * (lane + 32)] = uint8_t(kc >> 8);
-  const uint32_t vc = f32x2_to_e4m3x2(div_scale(bf16lo_to_f32(vw), vs, vr_inv),
-                                      div_scale(bf16hi_to_f32(vw), vs, vr_inv));
-  reinterpret_cast<uint16_t*>(vbuf + ((pb * Hkv + h) * B + t) * kHeadDim)[lane] = uint16_t(vc);
-  return true;
-}
-
 __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ AppendParams p) {
   // The decode-attention planner may launch now: it reads only positions and
   // the active mask, and waits for this grid before it exits.
@@ -125,11 +88,16 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ 
     const int64_t pb = slot / p.B;
     const int t = slot % p.B;
     const float kr_inv = exact_reciprocal(ks), vr_inv = exact_reciprocal(vs);
-    // packed K: tokens 2p and 2p+1 interleaved per channel; head h is (B/2) pair rows further
+    // packed K: tokens 2p and 2p+1 interleaved per channel (channel e at byte
+    // 2e of the pair row); plain K: laid out like V.  Either way a head's block
+    // is B * D bytes.
     uint8_t* kdst =
-        p.kb[i >> 1] + ((pb * p.Hkv + h0) * (p.B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1);
+        p.k_packed
+            ? p.kb[i >> 1] + ((pb * p.Hkv + h0) * (p.B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1)
+            : p.kb[i >> 1] + ((pb * p.Hkv + h0) * p.B + t) * kHeadDim;
+    const int estep = p.k_packed ? 2 : 1;
     uint8_t* vdst = p.vb[i >> 1] + ((pb * p.Hkv + h0) * p.B + t) * kHeadDim;
-    const int64_t kstride = int64_t(p.B >> 1) * (2 * kHeadDim), vstride = int64_t(p.B) * kHeadDim;
+    const int64_t kstride = int64_t(p.B) * kHeadDim, vstride = int64_t(p.B) * kHeadDim;
 #pragma unroll
     for (int k = 0; k < kAppendHeads; ++k) {
       if (k < nh) {
@@ -140,8 +108,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ 
         const float yr = __fadd_rn(__fmul_rn(y, c), __fmul_rn(x, s));
         const uint32_t kc =
             f32x2_to_e4m3x2(div_scale(xr, ks, kr_inv), div_scale(yr, ks, kr_inv));
-        kdst[k * kstride + 2 * lane] = uint8_t(kc & 0xffu);
-        kdst[k * kstride + 2 * (lane + 32)] = uint8_t(kc >> 8);
+        kdst[k * kstride + estep * lane] = uint8_t(kc & 0xffu);
+        kdst[k * kstride + estep * (lane + 32)] = uint8_t(kc >> 8);
         const uint32_t vc = f32x2_to_e4m3x2(div_scale(bf16lo_to_f32(vw[k]), vs, vr_inv),
                                             div_scale(bf16hi_to_f32(vw[k]), vs, vr_inv));
         reinterpret_cast<uint16_t*>(vdst + k * vstride)[lane] = uint16_t(vc);
@@ -499,7 +467,9 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int u, int4 e, 
 // kFused = true: the decode step's append is done by the units that read the
 // new token (gk_decode_step); a separate instantiation so that the plain
 // attention kernel keeps its own register allocation.
-template <bool kMma, bool kFused>
+// kPackedK: K through the packed view (tokens 2p, 2p+1 interleaved per
+// channel) or laid out like V.
+template <bool kMma, bool kFused, bool kPackedK>
 __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -864,18 +834,22 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         } else {
           const int64_t pb = ap_slot / p.B;
           const int t = ap_slot % p.B;
-          uint8_t* kdst = const_cast<uint8_t*>(p.kb[CU.layer >> 1]) +
-                          ((pb * p.Hkv + CU.kvh) * (p.B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1);
-          kdst[2 * lane] = uint8_t(ap_codes & 0xffu);
-          kdst[2 * (lane + 32)] = uint8_t((ap_codes >> 8) & 0xffu);
+          constexpr int es = kPackedK ? 2 : 1;  // byte step between channels of a K row
+          uint8_t* kdst =
+              const_cast<uint8_t*>(p.kb[CU.layer >> 1]) +
+              (kPackedK ? ((pb * p.Hkv + CU.kvh) * (p.B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1)
+                        : ((pb * p.Hkv + CU.kvh) * p.B + t) * kHeadDim);
+          kdst[es * lane] = uint8_t(ap_codes & 0xffu);
+          kdst[es * (lane + 32)] = uint8_t((ap_codes >> 8) & 0xffu);
           uint8_t* vdst = const_cast<uint8_t*>(p.vb[CU.layer >> 1]) +
                           ((pb * p.Hkv + CU.kvh) * p.B + t) * kHeadDim;
           reinterpret_cast<uint16_t*>(vdst)[lane] = uint16_t(ap_codes >> 16);
           const int tl = cd.t_end - 1 - tok0;
-          const uint32_t kp = Ks + (tl >> 1) * (2 * kHeadDim) + (tl & 1);
+          const uint32_t kp =
+              kPackedK ? Ks + (tl >> 1) * (2 * kHeadDim) + (tl & 1) : Ks + tl * kHeadDim;
           const uint16_t k0 = uint16_t(ap_codes & 0xffu), k1 = uint16_t((ap_codes >> 8) & 0xffu);
-          asm volatile("st.shared.u8 [%0], %1;" ::"r"(kp + 2 * lane), "h"(k0) : "memory");
-          asm volatile("st.shared.u8 [%0], %1;" ::"r"(kp + 2 * (lane + 32)), "h"(k1) : "memory");
+          asm volatile("st.shared.u8 [%0], %1;" ::"r"(kp + es * lane), "h"(k0) : "memory");
+          asm volatile("st.shared.u8 [%0], %1;" ::"r"(kp + es * (lane + 32)), "h"(k1) : "memory");
           asm volatile("st.shared.u16 [%0], %1;" ::"r"(Vs + tl * kHeadDim + 2 * lane),
                        "h"(uint16_t(ap_codes >> 16))
                        : "memory");
@@ -885,31 +859,53 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     }
 
     if constexpr (kMma) {
-    // ---- S = q' K^T for two 16-token tiles; rows (g, g+8) = tokens (2p, 2p+1)
+    // ---- S = q' K^T for two 16-token tiles; rows (g, g+8) = tokens (2g+sw, 2g+1-sw)
+    // of the tile, sw = 0 for packed K; for plain K sw = g & 1, so that lanes of
+    // odd g read their second token first and a quarter-warp's 16-byte reads
+    // fall in distinct banks (a relabelling of rows: nothing is moved).
+    const int sw = kPackedK ? 0 : (g & 1);
     float sc[2][4];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-      const uint32_t kp = Ks + (8 * i + g) * (2 * kHeadDim) + 32 * qd;
-      const uint4 w0 = lds128(kp);
-      const uint4 w1 = lds128(kp + 16);
-      const uint32_t kw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      if constexpr (kPackedK) {
+        const uint32_t kp = Ks + (8 * i + g) * (2 * kHeadDim) + 32 * qd;
+        const uint4 w0 = lds128(kp);
+        const uint4 w1 = lds128(kp + 16);
+        const uint32_t kw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t a0, a1, a2, a3;
-        e4m3x4_to_f16x2x2(prmt(kw[2 * j], 0u, 0x3120u), a0, a1);
-        e4m3x4_to_f16x2x2(prmt(kw[2 * j + 1], 0u, 0x3120u), a2, a3);
-        mma_f16(sc[i], a0, a1, a2, a3, qlo[2 * j], qlo[2 * j + 1]);
-        mma_f16(sc[i], a0, a1, a2, a3, qhi[2 * j], qhi[2 * j + 1]);
+        for (int j = 0; j < 4; ++j) {
+          uint32_t a0, a1, a2, a3;
+          e4m3x4_to_f16x2x2(prmt(kw[2 * j], 0u, 0x3120u), a0, a1);
+          e4m3x4_to_f16x2x2(prmt(kw[2 * j + 1], 0u, 0x3120u), a2, a3);
+          mma_f16(sc[i], a0, a1, a2, a3, qlo[2 * j], qlo[2 * j + 1]);
+          mma_f16(sc[i], a0, a1, a2, a3, qhi[2 * j], qhi[2 * j + 1]);
+        }
+      } else {
+        // channels 16qd..16qd+15 of the two tokens; word j = channels 16qd+4j..+3
+        const uint32_t kp = Ks + (16 * i + 2 * g) * kHeadDim + 16 * qd;
+        const uint4 r0 = lds128(kp + sw * kHeadDim);        // row g
+        const uint4 r1 = lds128(kp + (1 - sw) * kHeadDim);  // row g + 8
+        const uint32_t k0[4] = {r0.x, r0.y, r0.z, r0.w};
+        const uint32_t k1[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t a0, a1, a2, a3;
+          e4m3x4_to_f16x2x2(k0[j], a0, a2);
+          e4m3x4_to_f16x2x2(k1[j], a1, a3);
+          mma_f16(sc[i], a0, a1, a2, a3, qlo[2 * j], qlo[2 * j + 1]);
+          mma_f16(sc[i], a0, a1, a2, a3, qhi[2 * j], qhi[2 * j + 1]);
+        }
       }
     }
     // ---- online softmax (log2 domain); lane holds heads 2qd (c0,c2), 2qd+1 (c1,c3)
     if (edge) {
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
-        const int t0 = tok0 + 16 * i + 2 * g;
+        const int t0 = tok0 + 16 * i + 2 * g + sw;      // row g
+        const int t1 = tok0 + 16 * i + 2 * g + 1 - sw;  // row g + 8
         if (t0 < cd.t_begin || t0 >= cd.t_end) sc[i][0] = sc[i][1] = -INFINITY;
-        if (t0 + 1 < cd.t_begin || t0 + 1 >= cd.t_end) sc[i][2] = sc[i][3] = -INFINITY;
+        if (t1 < cd.t_begin || t1 >= cd.t_end) sc[i][2] = sc[i][3] = -INFINITY;
       }
     }
     const float lm0 = fmaxf(fmaxf(sc[0][0], sc[0][2]), fmaxf(sc[1][0], sc[1][2]));
@@ -951,7 +947,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       pr[i][2] = ex2(fmaf(sc[i][2], si0, nb0));
       pr[i][3] = ex2(fmaf(sc[i][3], si1, nb1));
     }
-    // ---- O += P V; rows (g, g+8) = channels (8g+2m, 8g+2m+1), k = tokens 4qd..4qd+3
+    // ---- O += P V; rows (g, g+8) = channels (8g+2m, 8g+2m+1), k = tokens 4qd..4qd+3:
+    // after the transpose b0 holds tokens (4qd, 4qd+2) and b1 (4qd+1, 4qd+3) for
+    // packed K; with the plain-K row order b0 holds (4qd, 4qd+3), b1 (4qd+1, 4qd+2)
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const uint32_t b0 = movmatrix_trans(f32x2_to_f16x2(pr[i][0], pr[i][1]));
@@ -969,14 +967,16 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
           if (t < cd.t_begin || t >= cd.t_end) v[r] = make_uint2(0u, 0u);
         }
       }
+      constexpr int r0a = 0, r0b = kPackedK ? 2 : 3;  // the tokens of b0: 4qd + r0a, 4qd + r0b
+      constexpr int r1a = 1, r1b = kPackedK ? 3 : 2;  // the tokens of b1
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const uint32_t sel = (m & 1) ? 0x7362u : 0x5140u;
-        const uint32_t e02 = prmt(m < 2 ? v[0].x : v[0].y, m < 2 ? v[2].x : v[2].y, sel);
-        const uint32_t e13 = prmt(m < 2 ? v[1].x : v[1].y, m < 2 ? v[3].x : v[3].y, sel);
+        const uint32_t e0 = prmt(m < 2 ? v[r0a].x : v[r0a].y, m < 2 ? v[r0b].x : v[r0b].y, sel);
+        const uint32_t e1 = prmt(m < 2 ? v[r1a].x : v[r1a].y, m < 2 ? v[r1b].x : v[r1b].y, sel);
         uint32_t a0, a1, a2, a3;
-        e4m3x4_to_f16x2x2(e02, a0, a1);
-        e4m3x4_to_f16x2x2(e13, a2, a3);
+        e4m3x4_to_f16x2x2(e0, a0, a1);
+        e4m3x4_to_f16x2x2(e1, a2, a3);
         mma_f16(o[m], a0, a1, a2, a3, b0, b1);
       }
     }
@@ -984,17 +984,23 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     if constexpr (!kMma) {
       // ---- S = q' K^T with fp32 FMA; lane = token t of the stage
       const int t = lane;
-      const uint32_t krow = Ks + (t >> 1) * (2 * kHeadDim);
+      const uint32_t krow = kPackedK ? Ks + (t >> 1) * (2 * kHeadDim) : Ks + t * kHeadDim;
       const uint32_t sel = (t & 1) ? 0x7531u : 0x6420u;  // this token's byte of each pair
       float sf[kGroup];
 #pragma unroll
       for (int h = 0; h < kGroup; ++h) sf[h] = 0.f;
 #pragma unroll 2
       for (int c = 0; c < kHeadDim / 8; ++c) {  // 8 channels per step
-        const uint4 w = lds128(krow + 16 * c);
         uint32_t h01, h23, h45, h67;
-        e4m3x4_to_f16x2x2(prmt(w.x, w.y, sel), h01, h23);
-        e4m3x4_to_f16x2x2(prmt(w.z, w.w, sel), h45, h67);
+        if constexpr (kPackedK) {
+          const uint4 w = lds128(krow + 16 * c);
+          e4m3x4_to_f16x2x2(prmt(w.x, w.y, sel), h01, h23);
+          e4m3x4_to_f16x2x2(prmt(w.z, w.w, sel), h45, h67);
+        } else {
+          const uint2 w = lds64(krow + 8 * c);
+          e4m3x4_to_f16x2x2(w.x, h01, h23);
+          e4m3x4_to_f16x2x2(w.y, h45, h67);
+        }
         const float2 k01 = f16x2_to_f32x2(h01), k23 = f16x2_to_f32x2(h23);
         const float2 k45 = f16x2_to_f32x2(h45), k67 = f16x2_to_f32x2(h67);
 #pragma unroll
@@ -1261,6 +1267,13 @@ struct DeviceCache {
 };
 static DeviceCache g_cache[64];
 
+// Attention instantiations, index = fma * 4 + fused * 2 + plain_k.
+static const void* const kAttnKernels[8] = {
+    (const void*)attn_kernel<true, false, true>,   (const void*)attn_kernel<true, false, false>,
+    (const void*)attn_kernel<true, true, true>,    (const void*)attn_kernel<true, true, false>,
+    (const void*)attn_kernel<false, false, true>,  (const void*)attn_kernel<false, false, false>,
+    (const void*)attn_kernel<false, true, true>,   (const void*)attn_kernel<false, true, false>};
+
 static cudaError_t device_setup(DeviceCache** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1272,32 +1285,24 @@ static cudaError_t device_setup(DeviceCache** out) {
     if (e != cudaSuccess) return e;
     const char* path = getenv("GK_ATTN_PATH");
     c.fma = path != nullptr && strcmp(path, "fma") == 0;
-    const void* kernels[4] = {(const void*)attn_kernel<true, false>,
-                              (const void*)attn_kernel<true, true>,
-                              (const void*)attn_kernel<false, false>,
-                              (const void*)attn_kernel<false, true>};
-    for (int k = 0; k < 4; ++k) {
-      e = cudaFuncSetAttribute(kernels[k], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               int(k < 2 ? attn_smem<true>() : attn_smem<false>()));
+    // every instantiation of the selected path is launched with the smallest
+    // occupancy among them, so that all fit the same persistent grid
+    c.attn_blocks_per_sm = 1 << 30;
+    for (int k = 0; k < 8; ++k) {
+      const bool mma = (k & 4) == 0;
+      const size_t smem = mma ? attn_smem<true>() : attn_smem<false>();
+      e = cudaFuncSetAttribute(kAttnKernels[k], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(smem));
       if (e != cudaSuccess) return e;
+      if (mma == c.fma) continue;
+      int blocks = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kAttnKernels[k], kWarps * 32,
+                                                        smem);
+      if (e != cudaSuccess) return e;
+      if (blocks < c.attn_blocks_per_sm) c.attn_blocks_per_sm = blocks;
     }
     e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(2 * kMaxBatch * sizeof(int32_t)));
-    if (e != cudaSuccess) return e;
-    // both instantiations of a path are launched with the occupancy of the
-    // plain one; the fused one must fit the same number of CTAs
-    int fused_blocks = 0;
-    e = c.fma ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                    &c.attn_blocks_per_sm, attn_kernel<false, false>, kWarps * 32, attn_smem<false>())
-              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                    &c.attn_blocks_per_sm, attn_kernel<true, false>, kWarps * 32, attn_smem<true>());
-    if (e != cudaSuccess) return e;
-    e = c.fma ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                    &fused_blocks, attn_kernel<false, true>, kWarps * 32, attn_smem<false>())
-              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                    &fused_blocks, attn_kernel<true, true>, kWarps * 32, attn_smem<true>());
-    if (e != cudaSuccess) return e;
-    if (fused_blocks < c.attn_blocks_per_sm) c.attn_blocks_per_sm = fused_blocks;
     if (e != cudaSuccess) return e;
     if (c.attn_blocks_per_sm < 1) c.attn_blocks_per_sm = 1;
     c.dev = dev;
@@ -1364,11 +1369,9 @@ cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaSt
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (p.fused)
-    return c->fma ? cudaLaunchKernelEx(&cfg, attn_kernel<false, true>, p)
-                  : cudaLaunchKernelEx(&cfg, attn_kernel<true, true>, p);
-  return c->fma ? cudaLaunchKernelEx(&cfg, attn_kernel<false, false>, p)
-                : cudaLaunchKernelEx(&cfg, attn_kernel<true, false>, p);
+  const int k = (c->fma ? 4 : 0) + (p.fused ? 2 : 0) + (p.k_packed ? 0 : 1);
+  void* args[] = {const_cast<AttnParams*>(&p)};
+  return cudaLaunchKernelExC(&cfg, kAttnKernels[k], args);
 }
 
 cudaError_t read_device_error(cudaStream_t st, uint32_t* bits, bool clear) {

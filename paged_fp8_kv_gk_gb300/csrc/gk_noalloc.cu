@@ -47,13 +47,12 @@ gk_status static_scratch_address(void** out) {
 }  // namespace
 
 extern "C" gk_status gk_decode_attn_stack_static(
-    const gk_shape* shape, const void* q, void* const* k_bufs, void* const* v_bufs,
-    const float* k_scale, const float* v_scale, const float* cos, const float* sin,
+    const gk_shape* shape, const void* q, const gk_kv_cache* kv, const float* k_scale, const float* v_scale, const float* cos, const float* sin,
     const int32_t* bt_full, const int32_t* bt_swa, const int32_t* pos, const int32_t* pos_w,
     const uint8_t* active, void* out, float* out_f32, void* stream) {
   const size_t need = gk_attn_workspace_min_bytes(shape);
   if (need == 0)  // invalid or unsupported shape: the regular entry point says which
-    return gk_decode_attn_stack(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, bt_full,
+    return gk_decode_attn_stack(shape, q, kv, k_scale, v_scale, cos, sin, bt_full,
                                 bt_swa, pos, pos_w, active, out, out_f32, nullptr, 0, stream);
   if (need > GK_STATIC_SCRATCH_BYTES) return GK_ERR_WORKSPACE;
   void* scratch = nullptr;
@@ -62,7 +61,7 @@ extern "C" gk_status gk_decode_attn_stack_static(
   // The planner rewrites the work-queue header and zeroes the split tickets
   // at the start of every call, so the previous call's contents need no
   // clearing here.
-  return gk_decode_attn_stack(shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, bt_full,
+  return gk_decode_attn_stack(shape, q, kv, k_scale, v_scale, cos, sin, bt_full,
                               bt_swa, pos, pos_w, active, out, out_f32, scratch,
                               GK_STATIC_SCRATCH_BYTES, stream);
 }

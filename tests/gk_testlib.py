@@ -50,9 +50,15 @@ def check_out(out_bf16: np.ndarray, out_f32, ref: np.ndarray, what: str = ""):
 
 
 class GpuStep:
-    """Inputs of one decode step resident on the GPU, plus the C-ABI calls."""
+    """Inputs of one decode step resident on the GPU, plus the C-ABI calls.
 
-    def __init__(self, w: gi.Workload, c: gi.Control, step: dict, cache, device="cuda"):
+    k_layout: gk.GK_K_PACKED or gk.GK_K_PLAIN (how the K bytes are laid out).
+    form: "per_group" (one [2, nb, kv, B, D] buffer per layer pair) or
+    "stacked" (K_cache and V_cache with a leading group axis).  Either way
+    ``self.cache[j]`` is group j's [2, nb, kv, B, D] (K half, V half)."""
+
+    def __init__(self, w: gi.Workload, c: gi.Control, step: dict, cache, device="cuda",
+                 k_layout: int = gk.GK_K_PACKED, form: str = "per_group"):
         self.w, self.c = w, c
         dev = torch.device(device)
         self.shape = gk.Shape.make(**gi.shape_dict(w, c))
@@ -71,8 +77,22 @@ class GpuStep:
         self.q = step["q"].to(dev).contiguous()
         self.k_new = step["k_new"].to(dev).contiguous()
         self.v_new = step["v_new"].to(dev).contiguous()
-        self.cache = [b.to(dev) for b in cache]
-        self.kb, self.vb = gk.split_group_buffers(self.cache)
+        self.k_layout, self.form = k_layout, form
+        if form == "per_group":
+            self.cache = [b.to(dev) for b in cache]
+            self.kv = gk.kv_from_group_buffers(self.cache, k_layout)
+        elif form == "stacked":
+            # [2, G, nb, kv, B, D]: K_cache = stack[0], V_cache = stack[1]
+            self.stack = torch.stack([torch.stack([b[0] for b in cache]),
+                                      torch.stack([b[1] for b in cache])]).to(dev)
+            self.cache = [self.stack[:, j] for j in range(len(cache))]
+            kc = self.stack[0]
+            if k_layout == gk.GK_K_PACKED:
+                G, nb, kv, B, D = kc.shape
+                kc = kc.view(G, nb, kv, B // 2, D, 2)
+            self.kv = gk.kv_stacked(kc, self.stack[1])
+        else:
+            raise ValueError(form)
         self.out = torch.empty(w.num_layers, w.batch, w.num_q_heads, w.head_dim,
                                dtype=torch.bfloat16, device=dev)
         self.out_f32 = torch.empty(self.out.shape, dtype=torch.float32, device=dev)
@@ -80,28 +100,29 @@ class GpuStep:
 
     def append(self, stream=None):
         gk.gk_kv_append(self.shape, self.k_new, self.v_new, self.cos, self.sin, self.k_scale,
-                        self.v_scale, self.upd_full, self.upd_swa, self.active, self.kb, self.vb,
+                        self.v_scale, self.upd_full, self.upd_swa, self.active, self.kv,
                         stream=stream)
 
     def step(self, workspace=None, out_f32=True, stream=None):
         """The fused step (gk_decode_step): append + attention in one launch."""
         gk.gk_decode_step(self.shape, self.q, self.k_new, self.v_new, self.cos, self.sin,
                           self.k_scale, self.v_scale, self.upd_full, self.upd_swa, self.bt_full,
-                          self.bt_swa, self.pos, self.pos_w, self.active, self.kb, self.vb,
+                          self.bt_swa, self.pos, self.pos_w, self.active, self.kv,
                           self.out, self.out_f32 if out_f32 else None,
                           self.workspace if workspace is None else workspace, stream=stream)
 
     def attention(self, workspace=None, out_f32=True, stream=None):
-        gk.gk_decode_attn_stack(self.shape, self.q, self.kb, self.vb, self.k_scale, self.v_scale,
+        gk.gk_decode_attn_stack(self.shape, self.q, self.kv, self.k_scale, self.v_scale,
                                 self.cos, self.sin, self.bt_full, self.bt_swa, self.pos,
                                 self.pos_w, self.active, self.out,
                                 self.out_f32 if out_f32 else None,
                                 self.workspace if workspace is None else workspace, stream=stream)
 
 
-def oracle_step(w: gi.Workload, c: gi.Control, step: dict, cache):
-    """Oracle append + attention on host copies. Returns (out fp64, k_bufs, v_bufs)."""
-    sh = oracle.make_shape(**gi.shape_dict(w, c))
+def oracle_step(w: gi.Workload, c: gi.Control, step: dict, cache, k_layout: int = 0):
+    """Oracle append + attention on host copies. Returns (out fp64, k_bufs, v_bufs).
+    k_layout: 0 packed K view, 1 unpacked K."""
+    sh = oracle.make_shape(**gi.shape_dict(w, c), k_layout=k_layout)
     kb = [b[0].cpu().numpy().reshape(-1).copy() for b in cache]
     vb = [b[1].cpu().numpy().reshape(-1).copy() for b in cache]
     st = oracle.kv_append(sh, gi.bf16_bits(step["k_new"]), gi.bf16_bits(step["v_new"]), c.cos,
@@ -124,14 +145,23 @@ def gather_row_pool(w: gi.Workload, c: gi.Control, cache, j: int, b: int):
 
 
 def oracle_row_pair(w: gi.Workload, c: gi.Control, step_host: dict, pre_cache, j: int, b: int,
-                    kvhs=None):
+                    kvhs=None, k_layout: int = 0):
     """Oracle outputs for layers 2j and 2j+1 of row b from the generator's
     pre-append cache (see oracle.rows)."""
     kp, vp = gather_row_pool(w, c, pre_cache, j, b)
-    return oracle_rows.row_pair_from_pool(w, c, step_host, kp, vp, j, b, kvhs)
+    return oracle_rows.row_pair_from_pool(w, c, step_host, kp, vp, j, b, kvhs, k_layout)
 
 
-def oracle_appended_codes(w: gi.Workload, c: gi.Control, step: dict):
+def _k_codes(kbuf, nb, Hkv, B, D, pb, h, t, k_layout):
+    """K codes [len(pb), len(h), D] at (pb, h, t) of a K half (numpy or torch)."""
+    if k_layout == 0:
+        kv = kbuf.reshape(nb, Hkv, B // 2, D, 2)
+        return kv[pb[:, None], h[None, :], (t // 2)[:, None], :, (t % 2)[:, None]]
+    kv = kbuf.reshape(nb, Hkv, B, D)
+    return kv[pb[:, None], h[None, :], t[:, None], :]
+
+
+def oracle_appended_codes(w: gi.Workload, c: gi.Control, step: dict, k_layout: int = 0):
     """Expected K and V codes of every (layer, row, kv head) the append writes:
     the oracle appends into a compact pool (row b's window layer writes block
     2b, its full layer block 2b+1, at the real in-block offset) and the codes
@@ -143,7 +173,7 @@ def oracle_appended_codes(w: gi.Workload, c: gi.Control, step: dict):
     upd_f = ((2 * np.arange(Bt) + 1) * B + off).astype(np.int32)
     sh = oracle.make_shape(num_layers=NL, batch=Bt, num_q_heads=w.num_q_heads, num_kv_heads=Hkv,
                            head_dim=D, block_size=B, num_blocks=2 * Bt, window=w.window,
-                           max_blocks_full=1, max_blocks_swa=c.max_blocks_swa)
+                           max_blocks_full=1, max_blocks_swa=c.max_blocks_swa, k_layout=k_layout)
     nbytes = 2 * Bt * Hkv * B * D
     kb = [np.zeros(nbytes, np.uint8) for _ in range(NL // 2)]
     vb = [np.zeros(nbytes, np.uint8) for _ in range(NL // 2)]
@@ -153,10 +183,9 @@ def oracle_appended_codes(w: gi.Workload, c: gi.Control, step: dict):
     kc = np.zeros((NL, Bt, Hkv, D), np.uint8)
     vc = np.zeros((NL, Bt, Hkv, D), np.uint8)
     for i in range(NL):
-        kview = kb[i // 2].reshape(2 * Bt, Hkv, B // 2, D, 2)
         vview = vb[i // 2].reshape(2 * Bt, Hkv, B, D)
         blk = 2 * np.arange(Bt) + (i % 2)
-        kc[i] = kview[blk[:, None], np.arange(Hkv)[None, :], (off // 2)[:, None], :, (off % 2)[:, None]]
+        kc[i] = _k_codes(kb[i // 2], 2 * Bt, Hkv, B, D, blk, np.arange(Hkv), off, k_layout)
         vc[i] = vview[blk[:, None], np.arange(Hkv)[None, :], off[:, None], :]
     return kc, vc
 
@@ -171,9 +200,9 @@ def device_appended_codes(g: GpuStep):
         upd = c.upd_swa if i % 2 == 0 else c.upd_full
         pb = torch.as_tensor((upd // B).astype(np.int64), device=g.cache[0].device)
         t = torch.as_tensor((upd % B).astype(np.int64), device=g.cache[0].device)
-        kview = g.cache[i // 2][0].view(c.num_blocks, Hkv, B // 2, D, 2)
         vview = g.cache[i // 2][1]
         hk = torch.arange(Hkv, device=pb.device)
-        kc[i] = kview[pb[:, None], hk[None, :], (t // 2)[:, None], :, (t % 2)[:, None]].cpu().numpy()
+        kc[i] = _k_codes(g.cache[i // 2][0], c.num_blocks, Hkv, B, D, pb, hk, t,
+                         g.k_layout).cpu().numpy()
         vc[i] = vview[pb[:, None], hk[None, :], t[:, None], :].cpu().numpy()
     return kc, vc

@@ -1,9 +1,14 @@
 """The C-ABI library builds, loads and exports every symbol include/gk.h
 declares; host-side argument validation returns the documented status before
-anything reaches the device.  No compute call is made (CPU only)."""
+anything reaches the device.  No compute call is made (CPU only).
+
+The validation tests hand the library fake device addresses together with one
+invalid argument; they run only where no CUDA device is visible, so that a
+validation bug can never turn one of them into a launch on real memory."""
 import ctypes
 
 import pytest
+import torch
 
 import gk_inputs as gi
 import paged_fp8_kv_gk_gb300 as gk
@@ -25,8 +30,33 @@ def test_library_exports_every_declared_symbol():
         assert callable(getattr(gk, name)), name
 
 
+no_device = pytest.mark.skipif(torch.cuda.is_available(),
+                               reason="fake device addresses: run only without a GPU")
+
+FAKE = 0x10000
+
+
+def _kv_struct(form="per_group", k_layout=gk.GK_K_PACKED, n=64, bad_index=None, k_addr=FAKE,
+               v_addr=FAKE):
+    """A gk_kv_cache over fake addresses (kept alive by the returned tuple)."""
+    c = gk.KvCacheC(k_layout=k_layout)
+    arrs = ()
+    if form in ("per_group", "both"):
+        ka = (ctypes.c_void_p * n)(*([FAKE] * n))
+        va = (ctypes.c_void_p * n)(*([FAKE] * n))
+        if bad_index is not None:
+            ka[bad_index] = None
+        c.k_bufs = ctypes.cast(ka, ctypes.c_void_p)
+        c.v_bufs = ctypes.cast(va, ctypes.c_void_p)
+        arrs = (ka, va)
+    if form in ("stacked", "both"):
+        c.k_cache = k_addr
+        c.v_cache = v_addr
+    return c, arrs
+
+
 def test_version_and_status_strings():
-    assert gk.gk_abi_version() == 1
+    assert gk.gk_abi_version() == 2
     names = [gk.gk_status_str(i) for i in range(7)]
     assert names == ["GK_OK", "GK_ERR_INVALID_ARG", "GK_ERR_UNSUPPORTED", "GK_ERR_WORKSPACE",
                      "GK_ERR_CUDA", "GK_ERR_DEVICE_BOUNDS", "GK_ERR_BUDGET"]
@@ -51,6 +81,7 @@ def test_workspace_sizes(name):
         assert rec == mn
 
 
+@no_device
 @pytest.mark.parametrize("over,status", [
     (dict(num_layers=3), gk.GK_ERR_INVALID_ARG),
     (dict(num_layers=0), gk.GK_ERR_INVALID_ARG),
@@ -68,19 +99,21 @@ def test_shape_validation(over, status):
     sh = _shape("gptoss_b64", **over)
     L = gk.lib()
     assert L.gk_attn_workspace_bytes(ctypes.byref(sh), None) == 0
-    fake = ctypes.c_void_p(0x10000)
-    ptrs = (ctypes.c_void_p * 64)(*([0x10000] * 64))
-    args = [fake] * 9 + [ctypes.cast(ptrs, ctypes.c_void_p)] * 2 + [None]
+    fake = ctypes.c_void_p(FAKE)
+    kvs, keep = _kv_struct()
+    args = [fake] * 9 + [ctypes.byref(kvs), None]
     assert L.gk_kv_append(ctypes.byref(sh), *args) == status
 
 
+@no_device
 def test_null_and_alignment_checks_before_launch():
     sh = _shape("gptoss_b64")
     L = gk.lib()
-    good = ctypes.c_void_p(0x10000)
-    ptrs = ctypes.cast((ctypes.c_void_p * 64)(*([0x10000] * 64)), ctypes.c_void_p)
+    good = ctypes.c_void_p(FAKE)
+    kvs, keep = _kv_struct()
+    kv = ctypes.byref(kvs)
     # append: one null tensor pointer
-    args = [good] * 9 + [ptrs, ptrs, None]
+    args = [good] * 9 + [kv, None]
     for i in range(9):
         a = list(args)
         a[i] = None
@@ -90,42 +123,92 @@ def test_null_and_alignment_checks_before_launch():
     a[0] = ctypes.c_void_p(0x10002)
     assert L.gk_kv_append(ctypes.byref(sh), *a) == gk.GK_ERR_INVALID_ARG
     # append: a null group buffer pointer
-    bad = (ctypes.c_void_p * 64)(*([0x10000] * 64))
-    bad[5] = None
+    badkv, keep2 = _kv_struct(bad_index=5)
     a = list(args)
-    a[9] = ctypes.cast(bad, ctypes.c_void_p)
+    a[9] = ctypes.byref(badkv)
     assert L.gk_kv_append(ctypes.byref(sh), *a) == gk.GK_ERR_INVALID_ARG
 
     # attention: nulls, then workspace checks (all before any launch)
-    att = [good, ptrs, ptrs] + [good] * 10 + [None, good]   # q..out, out_f32, workspace
+    att = [good, kv] + [good] * 10 + [None, good]   # q, kv, k_scale..out, out_f32, workspace
     ws_min = L.gk_attn_workspace_min_bytes(ctypes.byref(sh))
 
     def call(a, nbytes):
         return L.gk_decode_attn_stack(ctypes.byref(sh), *a, nbytes, None)
 
-    for i in range(13):
+    for i in range(12):
         a = list(att)
         a[i] = None
         assert call(a, ws_min) == gk.GK_ERR_INVALID_ARG, i
     a = list(att)
-    a[14] = None
+    a[13] = None
     assert call(a, ws_min) == gk.GK_ERR_WORKSPACE
     a = list(att)
-    a[14] = ctypes.c_void_p(0x10080)          # not 256-byte aligned
+    a[13] = ctypes.c_void_p(0x10080)          # not 256-byte aligned
     assert call(a, ws_min) == gk.GK_ERR_WORKSPACE
     assert call(att, ws_min - 256) == gk.GK_ERR_WORKSPACE
     a = list(att)
-    a[13] = ctypes.c_void_p(0x10004)          # misaligned out_f32
+    a[12] = ctypes.c_void_p(0x10004)          # misaligned out_f32
     assert call(a, ws_min) == gk.GK_ERR_INVALID_ARG
     assert L.gk_e4m3_quantize(None, ctypes.c_float(1.0), None, -1, None) == gk.GK_ERR_INVALID_ARG
 
 
+@no_device
+@pytest.mark.parametrize("case", ["both", "neither", "stacked_k_only", "layout_2",
+                                  "stacked_misaligned", "per_group_null"])
+def test_kv_form_exactly_one(case):
+    """The cache descriptor must hold exactly one form ("Kernel contract": the
+    kernel asserts that exactly one of per-group / stacked is present), with a
+    known K layout; everything else is refused on the host."""
+    sh = _shape("gptoss_b64")
+    L = gk.lib()
+    good = ctypes.c_void_p(FAKE)
+    if case == "both":
+        kvs, keep = _kv_struct("both")
+    elif case == "neither":
+        kvs, keep = _kv_struct("none")
+    elif case == "stacked_k_only":
+        kvs, keep = _kv_struct("stacked", v_addr=None)
+    elif case == "layout_2":
+        kvs, keep = _kv_struct("stacked", k_layout=2)
+    elif case == "stacked_misaligned":
+        kvs, keep = _kv_struct("stacked", k_addr=FAKE + 8)
+    else:
+        kvs, keep = _kv_struct("per_group", bad_index=17)
+    assert L.gk_kv_append(ctypes.byref(sh), *([good] * 9), ctypes.byref(kvs), None) == \
+        gk.GK_ERR_INVALID_ARG
+    ws_min = L.gk_attn_workspace_min_bytes(ctypes.byref(sh))
+    assert L.gk_decode_attn_stack(ctypes.byref(sh), good, ctypes.byref(kvs), *([good] * 10), None,
+                                  good, ws_min, None) == gk.GK_ERR_INVALID_ARG
+
+
+def test_binding_kv_forms_and_rank_inference():
+    """KvCache: exactly one form; packed-ness from the ranks as the page's bind
+    step infers it (k.dim() == v.dim() + 1); CPU tensors are refused."""
+    v = torch.zeros(4, 1, 16, 64, dtype=torch.uint8)
+    k_packed = torch.zeros(4, 1, 8, 64, 2, dtype=torch.uint8)
+    assert gk.infer_k_layout(k_packed, v) == gk.GK_K_PACKED
+    assert gk.infer_k_layout(v.clone(), v) == gk.GK_K_PLAIN
+    with pytest.raises(ValueError):
+        gk.infer_k_layout(torch.zeros(4, 1, 16, 64, 1, 1, dtype=torch.uint8), v)
+    with pytest.raises(ValueError, match="exactly one"):
+        gk.KvCache(k_bufs=[k_packed], v_bufs=[v], k_cache=k_packed, v_cache=v)
+    with pytest.raises(ValueError, match="exactly one"):
+        gk.KvCache()
+    with pytest.raises(ValueError, match="rank"):
+        gk.KvCache(k_bufs=[k_packed], v_bufs=[v], k_layout=gk.GK_K_PLAIN)
+    with pytest.raises(ValueError, match="one K layout"):
+        gk.KvCache(k_bufs=[k_packed, v.clone()], v_bufs=[v, v])
+    with pytest.raises(ValueError, match="CUDA"):
+        gk.KvCache(k_bufs=[k_packed], v_bufs=[v])
+
+
+@no_device
 def test_binding_refuses_cpu_tensors():
-    import torch
     sh = _shape("tiny")
     t = torch.zeros(16, dtype=torch.bfloat16)
+    kv = gk.KvCache(k_bufs=[FAKE], v_bufs=[FAKE], k_layout=gk.GK_K_PACKED)
     with pytest.raises(ValueError, match="CUDA"):
-        gk.gk_kv_append(sh, t, t, t, t, t, t, t, t, t, [t], [t], stream=0)
+        gk.gk_kv_append(sh, t, t, t, t, t, t, t, t, t, kv, stream=0)
 
 
 def test_testing_header_symbol_exported_and_validates():

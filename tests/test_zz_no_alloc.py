@@ -48,7 +48,7 @@ def test_static_scratch_matches_workspace_entry_point(name):
     for call in range(2):
         out = torch.full_like(g.out, float("nan"))
         out_f32 = torch.full_like(g.out_f32, float("nan"))
-        gk.gk_decode_attn_stack_static(g.shape, g.q, g.kb, g.vb, g.k_scale, g.v_scale, g.cos,
+        gk.gk_decode_attn_stack_static(g.shape, g.q, g.kv, g.k_scale, g.v_scale, g.cos,
                                        g.sin, g.bt_full, g.bt_swa, g.pos, g.pos_w, g.active, out,
                                        out_f32)
         torch.cuda.synchronize()
@@ -64,7 +64,9 @@ def test_static_scratch_rejects_shapes_beyond_its_size():
                        max_blocks_swa=5)
     assert gk.gk_attn_workspace_min_bytes(sh) > (16 << 20)
     good = ctypes.c_void_p(0x10000)
-    ptrs = ctypes.cast((ctypes.c_void_p * 64)(*([0x10000] * 64)), ctypes.c_void_p)
-    st = gk.lib().gk_decode_attn_stack_static(ctypes.byref(sh), good, ptrs, ptrs,
+    arr = (ctypes.c_void_p * 64)(*([0x10000] * 64))
+    kvs = gk.KvCacheC(k_bufs=ctypes.cast(arr, ctypes.c_void_p),
+                      v_bufs=ctypes.cast(arr, ctypes.c_void_p), k_layout=gk.GK_K_PACKED)
+    st = gk.lib().gk_decode_attn_stack_static(ctypes.byref(sh), good, ctypes.byref(kvs),
                                               *([good] * 10), None, None)
     assert st == gk.GK_ERR_WORKSPACE
