@@ -464,6 +464,89 @@ def run_gk(args):
         dist.destroy_process_group()
 
 
+def run_ingest(args):
+    """The DI landing copy (gk_kv_ingest) on its own: every block a batch of
+    prompts sends (both engines at N - 1) landed on a fresh decode cache, per
+    step.  value = bytes moved (read + write) per second, against the copy
+    bandwidth; e2e = the same landing read straight from pinned host memory."""
+    import torch
+    import paged_fp8_kv_gk_gb300 as gk
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dist = dist_init("nccl")
+    dev = torch.device("cuda", local_rank)
+    w = gi.get(args.workload)
+    c = gi.make_control(w)
+    truth = gi.make_cache(w, c, dev)
+    dr, db, src = gi.make_landing(w, c, truth)
+    del truth
+    cache = [torch.zeros(2, c.num_blocks, w.num_kv_heads, w.block_size, w.head_dim,
+                         dtype=torch.uint8, device=dev) for _ in range(w.num_layers // 2)]
+    kv = gk.kv_from_group_buffers(cache)
+    lk, lv = gk.layer_binding(kv, w.num_layers)
+    regions = gk.gk_kv_regions(gk.Shape.make(**gi.shape_dict(w, c)), lk, lv)
+    dr_t = torch.as_tensor(dr, device=dev)
+    db_t = torch.as_tensor(db, device=dev)
+    landed = src.numel()
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(source, K, W):
+        for _ in range(W):
+            gk.gk_kv_ingest(regions, dr_t, db_t, source, stream=stream)
+        torch.cuda.synchronize(dev)
+        if gk.gk_read_device_error() != 0:
+            raise RuntimeError("device error word set during warm-up")
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        for k in range(K):
+            e0[k].record(stream)
+            gk.gk_kv_ingest(regions, dr_t, db_t, source, stream=stream)
+            e1[k].record(stream)
+        torch.cuda.synchronize(dev)
+        return [e0[k].elapsed_time(e1[k]) for k in range(K)]
+
+    K, W = args.steps, args.warmup
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    clocks.mark_begin()
+    per = timed(src, K, W)
+    clocks.mark_end()
+    clk = clocks.stop()
+    ms = statistics.fmean(per)
+    max_ms, units = reduce_timing(sum(per), 2 * landed * K, dist, dev)
+    value = units / (max_ms / 1e3) / 1e9
+    host = src.cpu().pin_memory()
+    per_h = timed(host, max(3, K // 4), 2)
+    e2e_ms = statistics.fmean(per_h)
+    peak, peak_kind = measured_peaks()
+    achieved = 2 * landed / (ms / 1e3) / 1e9
+    line = {
+        "metric": "DI KV landing bandwidth (read + write bytes/s), 1 GB300", "value": round(value, 1),
+        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded gk_inputs workload)",
+        "config": dict(workload_config(w, c, f"inputs larger than L2: {landed / 1e9:.2f} GB landed "
+                                       "per step"), op="gk_kv_ingest", descriptors=int(dr.size),
+                       block_len=int(src.shape[1])),
+        "impl": "gk",
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peak_kind,
+                     "kernel": "ingest_kernel", "alg_bytes_per_launch": 2 * landed},
+        "e2e": {"value": round(landed / (e2e_ms / 1e3) / 1e9, 1), "unit": "GB/s landed",
+                "source": "pinned host memory read by the kernel", "h2d_bytes_per_step": landed,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": K,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
 def run_reference(args):
     """The oracle timed on the host cores: each step is one whole row of the
     workload (every layer pair, every kv head)."""
@@ -529,7 +612,10 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", default=None,
+                    help=f"default {DEFAULT_WORKLOAD} (--op step), di_ingest_b16 (--op ingest)")
+    ap.add_argument("--op", choices=["step", "ingest"], default="step",
+                    help="step: the decode step (headline); ingest: the DI landing copy alone")
     ap.add_argument("--impl", choices=["gk", "reference"], default="gk")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle CPU time for the cpu_baseline sample")
@@ -543,7 +629,13 @@ def main(argv=None):
     ap.add_argument("--ws-min", action="store_true",
                     help="use the minimum attention workspace (no split-KV chunks)")
     args = ap.parse_args(argv)
-    if args.impl == "reference":
+    if args.workload is None:
+        args.workload = "di_ingest_b16" if args.op == "ingest" else DEFAULT_WORKLOAD
+    if args.op == "ingest":
+        if args.impl == "reference":
+            raise SystemExit("--op ingest has no reference arm")
+        run_ingest(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gk(args)

@@ -123,6 +123,18 @@ REDUCED = {
     "block16_small": WORKLOADS["tiny"].replace(
         name="block16_small", num_layers=4, batch=5, num_q_heads=16, num_kv_heads=2,
         lengths="fixed:1,15,16,143,300", seed=17, num_blocks=None),
+    # DI landing: prompt lengths on both sides of N % B == B - 1 (143, 159 with
+    # N >= W; 127 below it), a one-token prompt and block-boundary lengths
+    "di_small": WORKLOADS["gptoss_b64"].replace(
+        name="di_small", num_layers=4, batch=8, block_size=16,
+        lengths="fixed:1,2,127,128,143,159,160,700", seed=25),
+}
+
+# KV landing measurement: 16 prompts of 8192 tokens at the 36-layer shapes
+# (about 2.4 GB of blocks landed per step).
+LANDING = {
+    "di_ingest_b16": WORKLOADS["gptoss_b64"].replace(
+        name="di_ingest_b16", batch=16, lengths="all:8192", seed=26),
 }
 
 
@@ -136,7 +148,7 @@ PROFILE = {
 
 
 def get(name: str) -> Workload:
-    for table in (WORKLOADS, REDUCED, PROFILE):
+    for table in (WORKLOADS, REDUCED, PROFILE, LANDING):
         if name in table:
             return table[name]
     raise KeyError(name)
@@ -306,6 +318,45 @@ def make_cache(w: Workload, c: Control, device="cpu", chunk: int = 1 << 27) -> L
                 blk[swa_ids_t] = _codes(swa_ids_t.numel() * per_blk, s_swa, g, device).view(-1, per_blk)
         bufs.append(buf)
     return bufs
+
+
+def make_landing(w: Workload, c: Control, cache: List[torch.Tensor]):
+    """DI landing inputs ("GPT-OSS-120B giga-kernel decode", section "DI wiring
+    (NIXL)"): the blocks a prefill engine sends for every active row b, a
+    prompt of N = L_b tokens whose last token the decode engine recomputes at
+    position N - 1 (both engines operate at N - 1), so keys 0 .. N-2:
+      * full layer: row blocks 0 .. ceil((N-1)/B) - 1 (entries of bt_full);
+      * window layer: the trimmed row's entries for keys max(0, N-W) .. N-2
+        (the row starts at block max(0, N-W) // B).
+    Regions: 2j = group j's K half, 2j + 1 its V half.  Returns
+    (dst_region int32 [n], dst_block int32 [n], src uint8 [n, block_len]) with
+    src taken from `cache` (the bytes the prefill engine holds), on its device."""
+    B, W = w.block_size, w.window
+    regs, blks = [], []
+    for b in range(w.batch):
+        if not c.active[b]:
+            continue
+        N = int(c.lengths[b])
+        nf = -(-(N - 1) // B)
+        lo = max(0, N - W)
+        ns = (N - 2) // B - lo // B + 1 if N - 2 >= lo else 0
+        ids = [int(x) for x in c.full_blocks[b][:nf]] + [int(x) for x in c.swa_blocks[b][:ns]]
+        for j in range(w.num_layers // 2):
+            for half in range(2):
+                regs += [2 * j + half] * len(ids)
+                blks += ids
+    dst_region = np.asarray(regs, np.int32)
+    dst_block = np.asarray(blks, np.int32)
+    per_blk = w.num_kv_heads * B * w.head_dim
+    dev = cache[0].device
+    src = torch.empty(len(regs), per_blk, dtype=torch.uint8, device=dev)
+    r_t = torch.as_tensor(dst_region, device=dev, dtype=torch.long)
+    b_t = torch.as_tensor(dst_block, device=dev, dtype=torch.long)
+    for r in range(2 * (w.num_layers // 2)):
+        sel = (r_t == r).nonzero().view(-1)
+        if sel.numel():
+            src[sel] = cache[r // 2][r % 2].view(c.num_blocks, per_blk).index_select(0, b_t[sel])
+    return dst_region, dst_block, src
 
 
 def kv_bytes_read(w: Workload, c: Control) -> int:

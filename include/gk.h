@@ -80,6 +80,7 @@ typedef enum {
 #define GK_DEVERR_POS 0x4u      /* a position is negative or beyond its table row */
 #define GK_DEVERR_TIMEOUT 0x8u  /* a shared-memory barrier wait hit its iteration limit */
 #define GK_DEVERR_PLAN 0x10u    /* the work plan did not fit the workspace */
+#define GK_DEVERR_INGEST 0x20u  /* an ingest descriptor names a region or block out of range: copy skipped */
 
 /* K layouts.  The page infers packed-ness from the K tensor's rank
  * (k.dim() == v.dim() + 1); across this ABI it is stated. */
@@ -273,6 +274,70 @@ gk_status gk_read_device_error(void *stream, uint32_t *bits, int clear);
 gk_status gk_kv_budget(uint64_t total_bytes, uint64_t used_bytes, double gpu_memory_utilization,
                        double cap_fraction, double min_budget_gib, const gk_shape *shape,
                        uint64_t *available_bytes, int64_t *num_blocks);
+
+/*
+ * Disaggregated-inference KV landing ("GPT-OSS-120B giga-kernel decode",
+ * section "DI wiring (NIXL)").  A prefill engine's KV blocks land on the group
+ * buffer block the decode kernel reads: each group buffer's K half and V half
+ * is one region of num_blocks blocks of block_len = kv * block * d bytes (one
+ * layer-pair block), and block b of a region is base + b * block_len.  The
+ * transport itself is not part of this library: gk_kv_ingest is the local
+ * landing copy that stands in for it.
+ */
+typedef struct {
+    void *base;         /* device address of block 0 */
+    uint64_t length;    /* bytes: num_blocks * block_len */
+    uint64_t block_len; /* bytes of one block: num_kv_heads * block_size * head_dim */
+} gk_kv_region;
+
+/*
+ * gk_kv_regions -- the region list of a per-layer KV binding (host only).
+ * Layers are taken in order 0..NL-1, each adding its K half and then its V
+ * half as a region unless a region with the same base address is already
+ * listed: buffers shared by paired layers are de-duplicated by base address,
+ * which for the page's layout gives 2 * NL/2 regions K_0, V_0, K_1, V_1, ...
+ * layer_k, layer_v: HOST arrays of NL device addresses (16-byte aligned), the
+ * K and V halves layer i is bound to.  out: HOST array of `capacity` regions.
+ * *count receives the number of distinct regions even when it exceeds
+ * capacity (then GK_ERR_INVALID_ARG and only `capacity` are written).
+ */
+gk_status gk_kv_regions(const gk_shape *shape, void *const *layer_k, void *const *layer_v,
+                        gk_kv_region *out, int32_t capacity, int32_t *count);
+
+/*
+ * gk_kv_ingest -- land n transferred blocks: for d in [0, n), copy block_len
+ * bytes from src + d * block_len to regions[dst_region[d]].base +
+ * dst_block[d] * block_len.
+ *   regions: HOST array of n_regions (<= 128) regions sharing one block_len
+ *            (a multiple of 16); dst_region, dst_block: DEVICE int32 [n];
+ *   src:     n * block_len bytes, 16-byte aligned, in device memory or in host
+ *            memory the device can address (pinned, mapped); plain pageable
+ *            host memory is refused with GK_ERR_INVALID_ARG.
+ * Descriptors must name distinct destination blocks (the copies run
+ * concurrently).  A descriptor whose region or block is out of range is
+ * skipped on the device and sets GK_DEVERR_INGEST.  n == 0 enqueues nothing.
+ */
+gk_status gk_kv_ingest(const gk_kv_region *regions, int32_t n_regions, const int32_t *dst_region,
+                       const int32_t *dst_block, int64_t n, const void *src, void *stream);
+
+/*
+ * gk_di_blocks -- which of a prompt's blocks the decode engine needs
+ * (host only; "DI wiring (NIXL)", the sliding-window truncation fix: both
+ * engines operate at N - 1).  For a prompt of N >= 1 tokens whose last token
+ * the decode engine recomputes at position N - 1, the transferred keys are
+ * positions 0 .. N-2:
+ *   full layers:   row blocks [0, *full_count),  full_count = ceil((N - 1) / B);
+ *   window layers: row blocks [*swa_first, *swa_first + *swa_count) (absolute
+ *                  block numbers), the blocks of keys max(0, N - W) .. N - 2,
+ *                  i.e. the window of position N - 1 without the new token;
+ *                  swa_first = max(0, N - W) / B.
+ * Computing the window for length N instead (keys from N - W + 1) drops block
+ * swa_first exactly when N >= W and N % B == B - 1 (for B dividing W): the
+ * block the page's fix keeps.  GK_ERR_INVALID_ARG for N < 1, B < 1, W < 1 or
+ * null outputs.
+ */
+gk_status gk_di_blocks(int64_t num_tokens, int32_t block_size, int32_t window,
+                       int64_t *full_count, int64_t *swa_first, int64_t *swa_count);
 
 /* Human-readable name of a status code (static string). */
 const char *gk_status_str(gk_status status);

@@ -82,6 +82,14 @@ def lib():
             L.ora_attn_one_ex.restype = ctypes.c_int
             L.ora_attn_one_ex.argtypes = ([ctypes.POINTER(Shape)] + [vp] * 12
                                           + [i32, i32, i32, i32, vp])
+            L.ora_kv_regions.restype = i32
+            L.ora_kv_regions.argtypes = [i32, vp, vp, vp]
+            L.ora_kv_ingest.restype = i64
+            L.ora_kv_ingest.argtypes = [vp, vp, i32, i64, vp, vp, i64, vp]
+            L.ora_di_blocks.restype = None
+            L.ora_di_blocks.argtypes = [i64, i32, i32, ctypes.POINTER(ctypes.c_int64),
+                                        ctypes.POINTER(ctypes.c_int64),
+                                        ctypes.POINTER(ctypes.c_int64)]
             _lib = L
     return _lib
 
@@ -207,3 +215,36 @@ def attn_one(shape: Shape, q, kbuf, vbuf, k_scale, v_scale, cos, sin, bt_full, b
     st = lib().ora_attn_one_ex(ctypes.byref(shape), *[_p(a) for a in arrs], layer, b, kvh,
                                nsplit, _p(out))
     return out, st
+
+
+# ---------------------------------------------------------------- DI landing
+def kv_regions(bases_k, bases_v) -> list:
+    """Per-layer K/V base addresses -> the de-duplicated region bases, in order."""
+    k = _c(np.asarray(bases_k, np.uint64), np.uint64)
+    v = _c(np.asarray(bases_v, np.uint64), np.uint64)
+    out = np.zeros(2 * k.size, np.uint64)
+    n = lib().ora_kv_regions(k.size, _p(k), _p(v), _p(out))
+    return [int(x) for x in out[:n]]
+
+
+def kv_ingest(regions, block_len: int, dst_region, dst_block, src) -> int:
+    """Landing copy into ``regions`` (writeable contiguous uint8 arrays, each a
+    whole number of blocks), in place; returns the descriptors skipped."""
+    for a in regions:
+        if not (a.flags["C_CONTIGUOUS"] and a.dtype == np.uint8 and a.flags["WRITEABLE"]):
+            raise TypeError("regions must be writeable contiguous uint8 arrays")
+    nblocks = np.array([a.size // block_len for a in regions], np.int64)
+    dr = _c(np.asarray(dst_region, np.int32), np.int32)
+    db = _c(np.asarray(dst_block, np.int32), np.int32)
+    src = _c(np.asarray(src, np.uint8).reshape(-1), np.uint8)
+    ptrs = _ptr_array(regions)
+    return int(lib().ora_kv_ingest(ctypes.cast(ptrs, ctypes.c_void_p), _p(nblocks), len(regions),
+                                   int(block_len), _p(dr), _p(db), dr.size, _p(src)))
+
+
+def di_blocks(num_tokens: int, block_size: int, window: int):
+    """(full_count, swa_first, swa_count) for a prompt of num_tokens tokens."""
+    a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    lib().ora_di_blocks(int(num_tokens), int(block_size), int(window), ctypes.byref(a),
+                        ctypes.byref(b), ctypes.byref(c))
+    return a.value, b.value, c.value

@@ -8,7 +8,8 @@
  *
  * Sources it follows (each function names its own):
  *   [GK]  "GPT-OSS-120B giga-kernel decode", sections "Kernel contract",
- *         "KV-cache layout (per-buffer, HMA-preserving)", "DI wiring (NIXL)".
+ *         "KV-cache layout (per-buffer, HMA-preserving)", "DI wiring (NIXL)"
+ *         (region list, landing copy, the N - 1 window rule).
  *   [OCP] OCP 8-bit floating point specification, E4M3 format (the "fn" variant:
  *         no infinities, one NaN pattern per sign, largest finite 448).
  *   [SDPA] scaled dot-product attention, softmax(q.k / sqrt(d)) . v, the plain
@@ -481,4 +482,69 @@ int ora_attn_one_ex(const ora_shape *sh, const uint16_t *q, const uint8_t *kbuf,
     in.pos_w = pos_w;
     in.active = active;
     return ora_attn_one(sh, &in, layer, b, kvh, nsplit, out);
+}
+
+/* ------------------------------------------------------------------------- */
+/* DI landing [GK DI wiring (NIXL)]                                           */
+/* ------------------------------------------------------------------------- */
+
+/* Regions of a per-layer binding: layers in order, each contributing its K
+ * half and then its V half unless that base address is already a region
+ * (paired layers share one group buffer).  bases_k/bases_v: NL addresses as
+ * integers.  out: room for 2*NL entries.  Returns the region count. */
+int32_t ora_kv_regions(int32_t NL, const uint64_t *bases_k, const uint64_t *bases_v, uint64_t *out)
+{
+    int32_t n = 0;
+    for (int32_t i = 0; i < NL; ++i) {
+        uint64_t two[2];
+        two[0] = bases_k[i];
+        two[1] = bases_v[i];
+        for (int h = 0; h < 2; ++h) {
+            int seen = 0;
+            for (int32_t k = 0; k < n; ++k)
+                if (out[k] == two[h])
+                    seen = 1;
+            if (!seen)
+                out[n++] = two[h];
+        }
+    }
+    return n;
+}
+
+/* The landing copy: descriptor d moves block_len bytes from src + d*block_len
+ * to block dst_block[d] of region dst_region[d], i.e. to
+ * region_base + dst_block[d]*block_len.  regions[r] points at region r's
+ * bytes (nblocks[r] blocks).  A descriptor out of range is skipped; returns
+ * the number skipped. */
+int64_t ora_kv_ingest(uint8_t *const *regions, const int64_t *nblocks, int32_t n_regions,
+                      int64_t block_len, const int32_t *dst_region, const int32_t *dst_block,
+                      int64_t n, const uint8_t *src)
+{
+    int64_t skipped = 0;
+    for (int64_t d = 0; d < n; ++d) {
+        int32_t r = dst_region[d], b = dst_block[d];
+        if (r < 0 || r >= n_regions || b < 0 || b >= nblocks[r]) {
+            ++skipped;
+            continue;
+        }
+        for (int64_t x = 0; x < block_len; ++x)
+            regions[r][(int64_t)b * block_len + x] = src[d * block_len + x];
+    }
+    return skipped;
+}
+
+/* Blocks a decode engine needs for a prompt of N tokens when both engines
+ * operate at N - 1 (the sliding-window DI truncation fix): the decode step
+ * recomputes position N - 1, so keys 0 .. N-2 are transferred.  Full layers
+ * hold them in row blocks 0 .. ceil((N-1)/B) - 1; a window layer attends from
+ * position N - 1 to keys max(0, N-W) .. N-1, of which N-1 is recomputed, so it
+ * needs the blocks of keys max(0, N-W) .. N-2. */
+void ora_di_blocks(int64_t N, int32_t B, int32_t W, int64_t *full_count, int64_t *swa_first,
+                   int64_t *swa_count)
+{
+    int64_t first_key = N - W > 0 ? N - W : 0;
+    int64_t last_key = N - 2;
+    *full_count = (N - 1 + B - 1) / B;
+    *swa_first = first_key / B;
+    *swa_count = last_key >= first_key ? last_key / B - first_key / B + 1 : 0;
 }

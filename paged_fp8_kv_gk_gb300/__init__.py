@@ -8,8 +8,8 @@ on a CUDA device, the calls raise.
 The functions carry the C names: ``gk_kv_append``, ``gk_decode_attn_stack``,
 ``gk_decode_step``, ``gk_decode_attn_stack_static``,
 ``gk_attn_workspace_bytes``, ``gk_attn_workspace_min_bytes``,
-``gk_e4m3_quantize``, ``gk_kv_budget``, ``gk_read_device_error``, ``gk_status_str``,
-``gk_abi_version``.  Tensors are torch tensors; the stream defaults to torch's
+``gk_e4m3_quantize``, ``gk_kv_budget``, ``gk_kv_regions``, ``gk_kv_ingest``,
+``gk_di_blocks``, ``gk_read_device_error``, ``gk_status_str``, ``gk_abi_version``.  Tensors are torch tensors; the stream defaults to torch's
 current stream on the tensors' device.  The cache is a ``KvCache``: per-group
 K and V buffers or stacked ``K_cache`` / ``V_cache``, exactly one of the two,
 with packed-ness read from the K tensors' rank as the "GPT-OSS-120B giga-kernel
@@ -27,8 +27,8 @@ from . import build as _build
 
 GK_OK, GK_ERR_INVALID_ARG, GK_ERR_UNSUPPORTED, GK_ERR_WORKSPACE, GK_ERR_CUDA, \
     GK_ERR_DEVICE_BOUNDS, GK_ERR_BUDGET = range(7)
-GK_DEVERR_SLOT, GK_DEVERR_BLOCK, GK_DEVERR_POS, GK_DEVERR_TIMEOUT, GK_DEVERR_PLAN = \
-    0x1, 0x2, 0x4, 0x8, 0x10
+GK_DEVERR_SLOT, GK_DEVERR_BLOCK, GK_DEVERR_POS, GK_DEVERR_TIMEOUT, GK_DEVERR_PLAN, \
+    GK_DEVERR_INGEST = 0x1, 0x2, 0x4, 0x8, 0x10, 0x20
 GK_K_PACKED, GK_K_PLAIN = 0, 1
 
 HEADER = os.path.join(_build.INCLUDE, "gk.h")
@@ -52,6 +52,12 @@ class Shape(ctypes.Structure):
     @classmethod
     def make(cls, **kw) -> "Shape":
         return cls(**{k: int(v) for k, v in kw.items()})
+
+
+class KvRegion(ctypes.Structure):
+    """gk_kv_region: one DI landing region (a group buffer's K or V half)."""
+    _fields_ = [("base", ctypes.c_void_p), ("length", ctypes.c_uint64),
+                ("block_len", ctypes.c_uint64)]
 
 
 class KvCacheC(ctypes.Structure):
@@ -211,6 +217,13 @@ def lib(build_if_needed: bool = True) -> ctypes.CDLL:
                                        ctypes.c_double, ctypes.c_double, sp,
                                        ctypes.POINTER(ctypes.c_uint64),
                                        ctypes.POINTER(ctypes.c_int64)]
+            L.gk_kv_regions.restype = ctypes.c_int
+            L.gk_kv_regions.argtypes = [sp, vp, vp, ctypes.POINTER(KvRegion), i32,
+                                        ctypes.POINTER(ctypes.c_int32)]
+            L.gk_kv_ingest.restype = ctypes.c_int
+            L.gk_kv_ingest.argtypes = [ctypes.POINTER(KvRegion), i32, vp, vp, i64, vp, vp]
+            L.gk_di_blocks.restype = ctypes.c_int
+            L.gk_di_blocks.argtypes = [i64, i32, i32] + [ctypes.POINTER(ctypes.c_int64)] * 3
             L.gk_selftest_wait_timeout.restype = ctypes.c_int
             L.gk_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp,
                                                    ctypes.POINTER(ctypes.c_uint32)]
@@ -385,6 +398,72 @@ def gk_kv_budget(total_bytes: int, used_bytes: int, gpu_memory_utilization: floa
     if st not in (GK_OK, GK_ERR_BUDGET):
         raise GkError(st, "gk_kv_budget")
     return st, int(avail.value), (int(nb.value) if shape is not None else None)
+
+
+def layer_binding(kv: KvCache, num_layers: int):
+    """The per-layer binding of a KvCache (layer i -> group buffer i // 2), as
+    device addresses: (layer_k, layer_v), each a list of num_layers ints."""
+    ks, vs = kv._keep
+    if kv.per_group:
+        kb = [_ptr(t, None, "k") for t in ks]
+        vb = [_ptr(t, None, "v") for t in vs]
+    else:
+        k, v = ks[0], vs[0]
+        G = k.shape[0]
+        half = k.numel() * k.element_size() // G
+        kb = [_ptr(k, None, "k_cache") + j * half for j in range(G)]
+        vb = [_ptr(v, None, "v_cache") + j * half for j in range(G)]
+    return [kb[i // 2] for i in range(num_layers)], [vb[i // 2] for i in range(num_layers)]
+
+
+def gk_kv_regions(shape, layer_k: Sequence[int], layer_v: Sequence[int]):
+    """De-duplicated DI regions of a per-layer binding (host only): a ctypes
+    array of KvRegion, K_0, V_0, K_1, V_1, ... for the page's layout."""
+    sh = _as_shape(shape)
+    n = len(layer_k)
+    if n != sh.num_layers or len(layer_v) != n:
+        raise ValueError("one K and one V address per layer")
+    ka = (ctypes.c_void_p * n)(*layer_k)
+    va = (ctypes.c_void_p * n)(*layer_v)
+    cap = 2 * n
+    out = (KvRegion * cap)()
+    cnt = ctypes.c_int32(0)
+    st = lib().gk_kv_regions(ctypes.byref(sh), ctypes.cast(ka, ctypes.c_void_p),
+                             ctypes.cast(va, ctypes.c_void_p), out, cap, ctypes.byref(cnt))
+    _check(st, "gk_kv_regions")
+    return (KvRegion * cnt.value)(*out[:cnt.value])
+
+
+def gk_kv_ingest(regions, dst_region, dst_block, src, stream=None) -> None:
+    """Land len(dst_region) blocks from ``src`` (device tensor or pinned host
+    tensor, n * block_len bytes) onto regions[dst_region[d]] block dst_block[d]."""
+    import torch
+    n = int(dst_region.numel())
+    if int(dst_block.numel()) != n:
+        raise ValueError("dst_region and dst_block must have one entry per descriptor")
+    if n == 0:
+        return
+    if not src.is_contiguous():
+        raise ValueError("src must be contiguous")
+    if src.is_cuda is False and not src.is_pinned():
+        raise ValueError("src must be a CUDA tensor or pinned host memory (no pageable copy)")
+    bl = int(regions[0].block_len)
+    if src.numel() * src.element_size() < n * bl:
+        raise ValueError(f"src holds {src.numel() * src.element_size()} bytes, need {n * bl}")
+    st = lib().gk_kv_ingest(regions, len(regions), _ptr(dst_region, torch.int32, "dst_region"),
+                            _ptr(dst_block, torch.int32, "dst_block"), n, src.data_ptr(),
+                            _stream(stream, dst_region))
+    _check(st, "gk_kv_ingest")
+
+
+def gk_di_blocks(num_tokens: int, block_size: int, window: int):
+    """(full_count, swa_first, swa_count): the row blocks a decode engine needs
+    for a prompt of num_tokens tokens, both engines operating at N - 1."""
+    a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    st = lib().gk_di_blocks(int(num_tokens), int(block_size), int(window), ctypes.byref(a),
+                            ctypes.byref(b), ctypes.byref(c))
+    _check(st, "gk_di_blocks")
+    return a.value, b.value, c.value
 
 
 def gk_selftest_wait_timeout(limit_ns: int, stream=None) -> int:

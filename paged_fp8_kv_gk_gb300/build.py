@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["gk_kernels.cu", "gk_api.cu", "gk_noalloc.cu"]
+SOURCES = ["gk_kernels.cu", "gk_api.cu", "gk_noalloc.cu", "gk_ingest.cu"]
 HEADERS = ["gk_device.cuh", "gk_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",

@@ -338,6 +338,96 @@ gk_status gk_kv_budget(uint64_t total_bytes, uint64_t used_bytes, double gmu, do
   return too_small ? GK_ERR_BUDGET : GK_OK;
 }
 
+gk_status gk_kv_regions(const gk_shape* shape, void* const* layer_k, void* const* layer_v,
+                        gk_kv_region* out, int32_t capacity, int32_t* count) {
+  const gk_status st = check_shape(shape);
+  if (st != GK_OK) return st;
+  if (!layer_k || !layer_v || !count || capacity < 0 || (capacity > 0 && !out))
+    return GK_ERR_INVALID_ARG;
+  const uint64_t block_len =
+      uint64_t(shape->num_kv_heads) * uint64_t(shape->block_size) * uint64_t(shape->head_dim);
+  const uint64_t length = uint64_t(shape->num_blocks) * block_len;
+  const void* seen[2 * 2 * kMaxGroups];
+  int n = 0;
+  for (int i = 0; i < shape->num_layers; ++i) {
+    for (int half = 0; half < 2; ++half) {
+      const void* a = half ? layer_v[i] : layer_k[i];
+      if (!a || !aligned16(a)) {
+        *count = 0;
+        return GK_ERR_INVALID_ARG;
+      }
+      bool dup = false;
+      for (int k = 0; k < n && !dup; ++k) dup = seen[k] == a;
+      if (dup) continue;
+      if (n < capacity) {
+        out[n].base = const_cast<void*>(a);
+        out[n].length = length;
+        out[n].block_len = block_len;
+      }
+      seen[n++] = a;
+    }
+  }
+  *count = n;
+  return n > capacity ? GK_ERR_INVALID_ARG : GK_OK;
+}
+
+gk_status gk_kv_ingest(const gk_kv_region* regions, int32_t n_regions, const int32_t* dst_region,
+                       const int32_t* dst_block, int64_t n, const void* src, void* stream) {
+  if (n < 0) return GK_ERR_INVALID_ARG;
+  if (n == 0) return GK_OK;
+  if (!regions || n_regions < 1 || n_regions > kMaxRegions || !dst_region || !dst_block || !src ||
+      !aligned16(src) || (reinterpret_cast<uintptr_t>(dst_region) & 3u) ||
+      (reinterpret_cast<uintptr_t>(dst_block) & 3u))
+    return GK_ERR_INVALID_ARG;
+  IngestParams p;
+  memset(&p, 0, sizeof(p));
+  const uint64_t block_len = regions[0].block_len;
+  if (block_len == 0 || (block_len & 15u) || block_len > (uint64_t(1) << 40))
+    return GK_ERR_INVALID_ARG;
+  for (int r = 0; r < n_regions; ++r) {
+    const gk_kv_region& g = regions[r];
+    if (g.block_len != block_len || !g.base || !aligned16(g.base) || g.length % block_len)
+      return GK_ERR_INVALID_ARG;
+    p.base[r] = static_cast<uint8_t*>(g.base);
+    p.nblocks[r] = int64_t(g.length / block_len);
+  }
+  // The source must be memory the device can address: device memory, or host
+  // memory that is pinned and mapped (translated to its device address).
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, src) != cudaSuccess) {
+    cudaGetLastError();
+    return GK_ERR_INVALID_ARG;
+  }
+  const void* dsrc = nullptr;
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    dsrc = src;
+  } else if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+    dsrc = a.devicePointer;
+  } else {
+    return GK_ERR_INVALID_ARG;
+  }
+  p.src = static_cast<const uint8_t*>(dsrc);
+  p.dst_region = dst_region;
+  p.dst_block = dst_block;
+  p.n = n;
+  p.block_len = int64_t(block_len);
+  p.n_regions = n_regions;
+  return launch_ingest(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GK_OK : GK_ERR_CUDA;
+}
+
+gk_status gk_di_blocks(int64_t num_tokens, int32_t block_size, int32_t window,
+                       int64_t* full_count, int64_t* swa_first, int64_t* swa_count) {
+  if (num_tokens < 1 || block_size < 1 || window < 1 || !full_count || !swa_first || !swa_count)
+    return GK_ERR_INVALID_ARG;
+  // both engines operate at N - 1: transferred keys are 0 .. N-2
+  const int64_t last = num_tokens - 2;
+  *full_count = (num_tokens - 1 + block_size - 1) / block_size;
+  const int64_t lo = num_tokens - window > 0 ? num_tokens - window : 0;  // window of N - 1
+  *swa_first = lo / block_size;
+  *swa_count = last >= lo ? last / block_size - *swa_first + 1 : 0;
+  return GK_OK;
+}
+
 gk_status gk_e4m3_quantize(const float* x, float scale, uint8_t* codes, int64_t n, void* stream) {
   if (n < 0 || (n > 0 && (!x || !codes))) return GK_ERR_INVALID_ARG;
   return launch_quantize(x, scale, codes, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -357,6 +447,9 @@ gk_status gk_read_device_error(void* stream, uint32_t* bits, int clear) {
   *bits = 0;
   if (read_device_error(static_cast<cudaStream_t>(stream), bits, clear != 0) != cudaSuccess)
     return GK_ERR_CUDA;
+  uint32_t ingest_bits = 0;
+  if (read_ingest_error(&ingest_bits, clear != 0) != cudaSuccess) return GK_ERR_CUDA;
+  *bits |= ingest_bits;
   return *bits ? GK_ERR_DEVICE_BOUNDS : GK_OK;
 }
 

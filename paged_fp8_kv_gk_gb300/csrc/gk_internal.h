@@ -102,6 +102,19 @@ struct AttnParams {
   int NL, Bt, Hq, Hkv, B, nb, W, MBF, MBS;
 };
 
+constexpr int kMaxRegions = 2 * kMaxGroups;
+
+struct IngestParams {
+  uint8_t* base[kMaxRegions];
+  int64_t nblocks[kMaxRegions];
+  const int32_t* dst_region;
+  const int32_t* dst_block;
+  const uint8_t* src;
+  int64_t n;
+  int64_t block_len;
+  int n_regions;
+};
+
 // Launchers (gk_kernels.cu).  They return the launch status.
 cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
 cudaError_t launch_quantize(const float* x, float scale, uint8_t* codes, int64_t n, cudaStream_t st);
@@ -110,5 +123,9 @@ cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaSt
 int attention_resident_warps();
 cudaError_t read_device_error(cudaStream_t st, uint32_t* bits, bool clear);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t st);
+// gk_ingest.cu: the landing copy and its own device error word (read after
+// the stream has been synchronised).
+cudaError_t launch_ingest(const IngestParams& p, cudaStream_t st);
+cudaError_t read_ingest_error(uint32_t* bits, bool clear);
 
 }  // namespace gk

@@ -16,7 +16,7 @@ import paged_fp8_kv_gk_gb300 as gk
 EXPECTED = {"gk_kv_append", "gk_attn_workspace_bytes", "gk_attn_workspace_min_bytes",
             "gk_decode_attn_stack", "gk_e4m3_quantize", "gk_read_device_error",
             "gk_status_str", "gk_abi_version", "gk_decode_attn_stack_static", "gk_kv_budget",
-            "gk_decode_step"}
+            "gk_decode_step", "gk_kv_regions", "gk_kv_ingest", "gk_di_blocks"}
 
 
 def test_header_declares_the_boundary():
