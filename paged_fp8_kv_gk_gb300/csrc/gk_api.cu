@@ -264,6 +264,9 @@ static gk_status decode_attention(const gk_shape* shape, const void* q, const gk
   p.W = shape->window;
   p.MBF = shape->max_blocks_full;
   p.MBS = shape->max_blocks_swa;
+  p.fd_planes = make_fastdiv(uint32_t(shape->num_layers / 2) * uint32_t(shape->num_kv_heads));
+  p.fd_hkv = make_fastdiv(uint32_t(shape->num_kv_heads));
+  p.fd_nl = make_fastdiv(uint32_t(shape->num_layers));
 
   PlanParams pl;
   memset(&pl, 0, sizeof(pl));

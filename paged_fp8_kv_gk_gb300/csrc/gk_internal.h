@@ -22,6 +22,25 @@ constexpr int kMinSplit = 512;        // smallest split-KV chunk, tokens (power 
 constexpr int kMaxSplitsPerRow = 64;  // cap on chunks per (layer, row, kv head)
 constexpr int kPartialFloats = 2 * kGroup + kGroup * kHeadDim;  // m[8], l[8], o[8][64]
 
+// n / d for 0 <= n < 2^31 by multiply and shift (d >= 1 fixed per launch):
+// shift = ceil(log2 d), mul = floor(2^32 (2^shift - d) / d) + 1,
+// n / d = (umulhi(n, mul) + n) >> shift.
+struct FastDiv {
+  uint32_t mul, shift, d;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t s = 0;
+  while ((uint64_t(1) << s) < d) ++s;
+  const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << s) - d)) / d + 1;
+  return FastDiv{uint32_t(m), s, d};
+}
+#ifdef __CUDACC__
+__device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
+  const uint32_t hi = __umulhi(uint32_t(n), f.mul);
+  return int((hi + uint32_t(n)) >> f.shift);
+}
+#endif
+
 // Header words at the start of the attention workspace.
 enum HdrWord {
   kHdrQueue = 0,        // work counter (atomic)
@@ -100,6 +119,7 @@ struct AttnParams {
   int fused;
   int k_packed;  // 1: K through the packed view, 0: K laid out like V
   int NL, Bt, Hq, Hkv, B, nb, W, MBF, MBS;
+  FastDiv fd_planes, fd_hkv, fd_nl;  // (NL/2)*Hkv, Hkv, NL
 };
 
 constexpr int kMaxRegions = 2 * kMaxGroups;

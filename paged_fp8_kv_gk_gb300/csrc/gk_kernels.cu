@@ -420,10 +420,13 @@ struct alignas(128) WarpSmemT {
   float pbuf[kMma ? 4 : kStageTok * kGroup];
   uint32_t apbuf[32];  // fused step: the new token's codes per lane
   unsigned long long bar[kStages];
+  const uint8_t* pu_base[2];  // the producer unit's K and V bases (its kv head's bytes)
   UnitDesc fifo[kFifo];
 };
 static_assert(sizeof(WarpSmemT<true>) % 128 == 0 && sizeof(WarpSmemT<false>) % 128 == 0,
               "warp areas must stay 128-byte aligned");
+// 4 CTAs x 4 warps x 14 KB (+ 1 KB reserved per CTA) is the SM's 228 KB
+static_assert(sizeof(WarpSmemT<true>) <= 14336, "the MMA path must keep 16 warps per SM");
 static_assert(kStageBytes % 16 == 0 && kUnitHeadBytes % 16 == 0 && kStageKBytes % 16 == 0,
               "bulk-copy destinations must be 16-byte aligned");
 
@@ -444,8 +447,8 @@ __device__ __forceinline__ void zero_row(const AttnParams& p, int layer, int b, 
 // Unit u covers plane u % planes of work entry e = u / planes.
 __device__ __forceinline__ void decode_unit(const AttnParams& p, int u, int4 e, int planes,
                                             UnitDesc& d) {
-  const int pl = u - (u / planes) * planes;
-  const int j = pl / p.Hkv;
+  const int pl = u - fdiv(u, p.fd_planes) * planes;
+  const int j = fdiv(pl, p.fd_hkv);
   const bool swa = ((e.w >> 30) & 1) != 0;
   d.kind = swa ? 2 : 1;
   d.layer = swa ? 2 * j : 2 * j + 1;
@@ -500,7 +503,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     u_next = atomicAdd(p.queue, 1);
   }
   u_next = __shfl_sync(kFull, u_next, 0);
-  int4 e_next = u_next < nU ? p.edesc[u_next / planes] : make_int4(0, 0, 0, 0);
+  int4 e_next = u_next < nU ? p.edesc[fdiv(u_next, p.fd_planes)] : make_int4(0, 0, 0, 0);
   bool tn_ready = false;
   int32_t tbl_next = 0;
   int tbl_next_base = 0;
@@ -519,8 +522,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   int prod = 0, cons = 0;
   int f_head = 0, f_tail = 0;
   bool exhausted = false;
-  int pk = 0, pu_n_st = 0, pu_st_begin = 0, pu_layer = 0, pu_b = 0, pu_kvh = 0, pu_kind = 0,
-      pu_t_end = 0;
+  int pk = 0, pu_n_st = 0, pu_layer = 0, pu_b = 0, pu_kvh = 0, pu_t_end = 0, pu_kind = 0;
+  // the producer's unit, advanced stage by stage: block (row index) and key
+  // offset of the next stage (its K/V bases are in ws.pu_base)
+  int pu_blk = 0, pu_off = 0, p_slot = 0;
   int tbl_base = -1;
   int32_t tbl = 0;
   bool failed = false;
@@ -566,11 +571,12 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       }
       if (lane == 0) u_after = atomicAdd(p.queue, 1);
       u_next = __shfl_sync(kFull, u_after, 0);
-      e_next = u_next < nU ? p.edesc[u_next / planes] : make_int4(0, 0, 0, 0);
+      e_next = u_next < nU ? p.edesc[fdiv(u_next, p.fd_planes)] : make_int4(0, 0, 0, 0);
       tn_ready = false;
       if (u >= nU) {
         const int v = u - nU;
-        zero_row(p, v % p.NL, p.zero_list[v / p.NL], lane);
+        const int zr = fdiv(v, p.fd_nl);
+        zero_row(p, v - zr * p.NL, p.zero_list[zr], lane);
         continue;
       }
       decode_unit(p, u, e, planes, d);
@@ -595,12 +601,21 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       ++f_tail;
       pk = 0;
       pu_n_st = d.n_st;
-      pu_st_begin = d.st_begin;
       pu_layer = d.layer;
       pu_b = d.b;
       pu_kvh = d.kvh;
-      pu_kind = d.kind;
       pu_t_end = d.t_end;
+      pu_kind = d.kind;
+      {
+        const int tok = d.st_begin * kStageTok;
+        pu_blk = tok / p.B;
+        pu_off = tok - pu_blk * p.B;
+      }
+      if (lane == 0) {
+        const int64_t head = int64_t(d.kvh) * p.B * kHeadDim;
+        ws.pu_base[0] = p.kb[d.layer >> 1] + head;
+        ws.pu_base[1] = p.vb[d.layer >> 1] + head;
+      }
       q_free = false;
       pu_appends = kFused && d.s == d.ns - 1;
     } else if (!tn_ready && u_next < nU) {
@@ -613,62 +628,59 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     }
     const uint32_t head_bytes =
         pk == 0 ? kUnitHeadBytes + ((kFused && pu_appends) ? kNewKvBytes : 0u) : 0u;
-    const int tok0 = (pu_st_begin + pk) * kStageTok;
-    const int slot = prod % kStages;
-    const uint32_t dst = ring0 + slot * kStageBytes;
-    const uint32_t bar = bar0 + 8 * slot;
-    const int32_t* row = pu_kind == 1 ? p.bt_full + int64_t(pu_b) * p.MBF
-                                      : p.bt_swa + int64_t(pu_b) * p.MBS;
+    const uint32_t dst = ring0 + p_slot * kStageBytes;
+    const uint32_t bar = bar0 + 8 * p_slot;
+    const bool two = p.B < kStageTok;  // 16-token blocks: two per stage
     const int row_len = pu_kind == 1 ? p.MBF : p.MBS;
-    const uint8_t* kbase = p.kb[pu_layer >> 1];
-    const uint8_t* vbase = p.vb[pu_layer >> 1];
-    const int B = p.B;
-    const int blk = tok0 / B;
-    const int nblk = B >= kStageTok ? 1 : 2;
-    if (tbl_base < 0 || blk + nblk - 1 >= tbl_base + 32) {
-      tbl_base = blk;
-      const int idx = blk + lane;
+    if (tbl_base < 0 || pu_blk + (two ? 1 : 0) >= tbl_base + 32) {
+      const int32_t* row = pu_kind == 1 ? p.bt_full + int64_t(pu_b) * p.MBF
+                                        : p.bt_swa + int64_t(pu_b) * p.MBS;
+      tbl_base = pu_blk;
+      const int idx = pu_blk + lane;
       tbl = idx < row_len ? row[idx] : 0;
     }
-    if (B >= kStageTok) {
-      int32_t pb = __shfl_sync(kFull, tbl, blk - tbl_base);
-      if (pb < 0 || pb >= p.nb) {
-        if (lane == 0) set_error(GK_DEVERR_BLOCK);
-        pb = 0;
-      }
+    const int blk_bytes = p.Hkv * p.B * kHeadDim;  // one block of all kv heads
+    int32_t pb0 = __shfl_sync(kFull, tbl, pu_blk - tbl_base);
+    if (uint32_t(pb0) >= uint32_t(p.nb)) {
+      if (lane == 0) set_error(GK_DEVERR_BLOCK);
+      pb0 = 0;
+    }
+    if (!two) {
       if (lane == 0) {
-        const int64_t off = ((int64_t(pb) * p.Hkv + pu_kvh) * B + (tok0 - blk * B)) * kHeadDim;
+        const int64_t off = int64_t(pb0) * blk_bytes + pu_off * kHeadDim;
         mbar_arrive_expect_tx(bar, kStageBytes + head_bytes);
         if (head_bytes) issue_unit_head(bar);
-        bulk_g2s(dst, kbase + off, kStageKBytes, bar);
-        bulk_g2s(dst + kStageKBytes, vbase + off, kStageKBytes, bar);
+        bulk_g2s(dst, ws.pu_base[0] + off, kStageKBytes, bar);
+        bulk_g2s(dst + kStageKBytes, ws.pu_base[1] + off, kStageKBytes, bar);
       }
-    } else {  // 16-token blocks: two per stage
-      int32_t pb0 = __shfl_sync(kFull, tbl, blk - tbl_base);
-      int32_t pb1 = __shfl_sync(kFull, tbl, min(blk + 1 - tbl_base, 31));
-      const bool has1 = tok0 + B < pu_t_end;
-      if (pb0 < 0 || pb0 >= p.nb) {
-        if (lane == 0) set_error(GK_DEVERR_BLOCK);
-        pb0 = 0;
+      pu_off += kStageTok;
+      if (pu_off == p.B) {
+        pu_off = 0;
+        ++pu_blk;
       }
-      if (has1 && (blk + 1 >= row_len || pb1 < 0 || pb1 >= p.nb)) {
+    } else {
+      int32_t pb1 = __shfl_sync(kFull, tbl, min(pu_blk + 1 - tbl_base, 31));
+      const bool has1 = (pu_blk + 1) * p.B < pu_t_end;
+      if (has1 && (pu_blk + 1 >= row_len || uint32_t(pb1) >= uint32_t(p.nb))) {
         if (lane == 0) set_error(GK_DEVERR_BLOCK);
         pb1 = 0;
       }
       if (lane == 0) {
-        const uint32_t half = uint32_t(B) * kHeadDim;
+        const uint32_t half = uint32_t(p.B) * kHeadDim;
         mbar_arrive_expect_tx(bar, (has1 ? 4 * half : 2 * half) + head_bytes);
         if (head_bytes) issue_unit_head(bar);
-        const int64_t o0 = (int64_t(pb0) * p.Hkv + pu_kvh) * B * kHeadDim;
-        bulk_g2s(dst, kbase + o0, half, bar);
-        bulk_g2s(dst + kStageKBytes, vbase + o0, half, bar);
+        const int64_t o0 = int64_t(pb0) * blk_bytes;
+        bulk_g2s(dst, ws.pu_base[0] + o0, half, bar);
+        bulk_g2s(dst + kStageKBytes, ws.pu_base[1] + o0, half, bar);
         if (has1) {
-          const int64_t o1 = (int64_t(pb1) * p.Hkv + pu_kvh) * B * kHeadDim;
-          bulk_g2s(dst + half, kbase + o1, half, bar);
-          bulk_g2s(dst + kStageKBytes + half, vbase + o1, half, bar);
+          const int64_t o1 = int64_t(pb1) * blk_bytes;
+          bulk_g2s(dst + half, ws.pu_base[0] + o1, half, bar);
+          bulk_g2s(dst + kStageKBytes + half, ws.pu_base[1] + o1, half, bar);
         }
       }
+      pu_blk += 2;
     }
+    p_slot = p_slot == kStages - 1 ? 0 : p_slot + 1;
     ++pk;
     ++prod;
     return true;
@@ -683,6 +695,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   } cd;
 #define CU (ws.fifo[f_head % kFifo])
   int k_in_unit = 0;
+  int c_slot = 0;        // cons % kStages
+  uint32_t c_par = 0u;   // (cons / kStages) & 1
   uint32_t qhi[8], qlo[8];  // q' = qhi + qlo (f16 each): ~22-bit significand
   // Scores come out of the MMA as x * 2^e_h, x = logit in log2 units and
   // 2^e_h the per-head normalisation of q; si_h = 2^-e_h undoes it.  mr_h is
@@ -703,9 +717,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
 
   while (cons < prod) {
     // ---- wait for the stage (the unit's first stage also brings its q)
-    const int slot = cons % kStages;
+    const int slot = c_slot;
     const uint32_t bar = bar0 + 8 * slot;
-    const uint32_t parity = uint32_t(cons / kStages) & 1u;
+    const uint32_t parity = c_par;
     if (!mbar_wait_bounded(bar, parity, kWaitLimitNs)) failed = true;
     if (__any_sync(kFull, failed)) {
       failed = true;
@@ -1083,6 +1097,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     }
     __syncwarp();
     ++cons;
+    if (++c_slot == kStages) {
+      c_slot = 0;
+      c_par ^= 1u;
+    }
     ++k_in_unit;
     while (prod - cons < kStages && issue_next()) {
     }
