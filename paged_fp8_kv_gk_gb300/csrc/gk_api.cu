@@ -267,6 +267,7 @@ static gk_status decode_attention(const gk_shape* shape, const void* q, const gk
   p.fd_planes = make_fastdiv(uint32_t(shape->num_layers / 2) * uint32_t(shape->num_kv_heads));
   p.fd_hkv = make_fastdiv(uint32_t(shape->num_kv_heads));
   p.fd_nl = make_fastdiv(uint32_t(shape->num_layers));
+  p.fd_b = make_fastdiv(uint32_t(shape->block_size));
 
   PlanParams pl;
   memset(&pl, 0, sizeof(pl));

@@ -119,7 +119,7 @@ struct AttnParams {
   int fused;
   int k_packed;  // 1: K through the packed view, 0: K laid out like V
   int NL, Bt, Hq, Hkv, B, nb, W, MBF, MBS;
-  FastDiv fd_planes, fd_hkv, fd_nl;  // (NL/2)*Hkv, Hkv, NL
+  FastDiv fd_planes, fd_hkv, fd_nl, fd_b;  // (NL/2)*Hkv, Hkv, NL, B
 };
 
 constexpr int kMaxRegions = 2 * kMaxGroups;

@@ -421,6 +421,9 @@ struct alignas(128) WarpSmemT {
   uint32_t apbuf[32];  // fused step: the new token's codes per lane
   unsigned long long bar[kStages];
   const uint8_t* pu_base[2];  // the producer unit's K and V bases (its kv head's bytes)
+  // the producer unit's first stage is copied from key lo, its last stage up
+  // to key hi of their 32-key stages (its range rounded out to 8): lo | hi << 8
+  int pu_trim;
   UnitDesc fifo[kFifo];
 };
 static_assert(sizeof(WarpSmemT<true>) % 128 == 0 && sizeof(WarpSmemT<false>) % 128 == 0,
@@ -513,7 +516,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     const bool swa = ((e.w >> 30) & 1) != 0;
     const int32_t* row = swa ? p.bt_swa + int64_t(e.x) * p.MBS : p.bt_full + int64_t(e.x) * p.MBF;
     const int row_len = swa ? p.MBS : p.MBF;
-    base = ((e.y / kStageTok) * kStageTok) / p.B;
+    base = fdiv((e.y / kStageTok) * kStageTok, p.fd_b);
     const int idx = base + lane;
     return idx < row_len ? __ldg(row + idx) : 0;
   };
@@ -608,8 +611,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       pu_kind = d.kind;
       {
         const int tok = d.st_begin * kStageTok;
-        pu_blk = tok / p.B;
+        pu_blk = fdiv(tok, p.fd_b);
         pu_off = tok - pu_blk * p.B;
+        const int last = tok + (d.n_st - 1) * kStageTok;
+        if (lane == 0) ws.pu_trim = ((d.t_begin - tok) & ~7) | (((d.t_end - last + 7) & ~7) << 8);
       }
       if (lane == 0) {
         const int64_t head = int64_t(d.kvh) * p.B * kHeadDim;
@@ -646,12 +651,23 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       pb0 = 0;
     }
     if (!two) {
+      // a unit's first and last stages copy only the keys of its range
+      // (rounded out to 8): a window starting inside a stage reads at most 7
+      // keys before it instead of up to 31
+      uint32_t lo_b = 0, kbytes = kStageKBytes;
+      if (pk == 0 || pk == pu_n_st - 1) {
+        const int trim = ws.pu_trim;
+        const int lo = pk == 0 ? (trim & 0xff) : 0;
+        const int hi = pk == pu_n_st - 1 ? (trim >> 8) : kStageTok;
+        lo_b = uint32_t(lo) * kHeadDim;
+        kbytes = uint32_t(hi - lo) * kHeadDim;
+      }
       if (lane == 0) {
-        const int64_t off = int64_t(pb0) * blk_bytes + pu_off * kHeadDim;
-        mbar_arrive_expect_tx(bar, kStageBytes + head_bytes);
+        const int64_t off = int64_t(pb0) * blk_bytes + pu_off * kHeadDim + lo_b;
+        mbar_arrive_expect_tx(bar, 2 * kbytes + head_bytes);
         if (head_bytes) issue_unit_head(bar);
-        bulk_g2s(dst, ws.pu_base[0] + off, kStageKBytes, bar);
-        bulk_g2s(dst + kStageKBytes, ws.pu_base[1] + off, kStageKBytes, bar);
+        bulk_g2s(dst + lo_b, ws.pu_base[0] + off, kbytes, bar);
+        bulk_g2s(dst + kStageKBytes + lo_b, ws.pu_base[1] + off, kbytes, bar);
       }
       pu_off += kStageTok;
       if (pu_off == p.B) {
@@ -846,8 +862,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         if (ap_slot < 0 || int64_t(ap_slot) >= int64_t(p.nb) * p.B) {
           if (lane == 0) set_error(GK_DEVERR_SLOT);
         } else {
-          const int64_t pb = ap_slot / p.B;
-          const int t = ap_slot % p.B;
+          const int pbi = fdiv(ap_slot, p.fd_b);
+          const int64_t pb = pbi;
+          const int t = ap_slot - pbi * p.B;
           constexpr int es = kPackedK ? 2 : 1;  // byte step between channels of a K row
           uint8_t* kdst =
               const_cast<uint8_t*>(p.kb[CU.layer >> 1]) +
