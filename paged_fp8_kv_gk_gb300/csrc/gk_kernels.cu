@@ -394,7 +394,6 @@ struct UnitDesc {
   int32_t layer, b, kvh, s, ns;
   int32_t t_begin, t_end;  // key range [t_begin, t_end) in the table's frame
   int32_t st_begin, n_st;  // 32-token stages covering the range
-  int32_t slot;            // fused step: update slot of the unit's new token
 };
 
 // q of the unit's 8 heads (bf16) followed by its row's cos and sin (fp32),
@@ -424,6 +423,7 @@ struct alignas(128) WarpSmemT {
   // the producer unit's first stage is copied from key lo, its last stage up
   // to key hi of their 32-key stages (its range rounded out to 8): lo | hi << 8
   int pu_trim;
+  int32_t ap_slot[kFifo];  // fused step: update slot of each FIFO unit (copied asynchronously)
   UnitDesc fifo[kFifo];
 };
 static_assert(sizeof(WarpSmemT<true>) % 128 == 0 && sizeof(WarpSmemT<false>) % 128 == 0,
@@ -463,6 +463,63 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int u, int4 e, 
   d.t_end = e.z;
   d.st_begin = e.y / kStageTok;
   d.n_st = (e.z + kStageTok - 1) / kStageTok - d.st_begin;
+}
+
+// Fused step, kept out of line so that the stage loop's register allocation
+// is that of the plain kernel: (a) the new token's K and V codes from the rows
+// the unit's head copy brought, with gk_kv_append's arithmetic (lane l: k
+// channels l and l + 32 in the low half, v channels 2l, 2l + 1 in the high
+// half); (b) storing them at the update slot and into the staged copy.
+__device__ __noinline__ uint32_t fused_codes(const AttnParams& p, uint32_t qbuf0, int layer,
+                                             int lane) {
+  const uint32_t kr = qbuf0 + kUnitHeadBytes;
+  uint16_t kx16, ky16;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(kx16) : "r"(kr + 2 * lane));
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(ky16) : "r"(kr + 2 * (lane + 32)));
+  uint32_t vw, cb, sb;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(vw) : "r"(kr + kHeadDim * 2 + 4 * lane));
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(cb) : "r"(qbuf0 + kQBytes + 4 * lane));
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sb) : "r"(qbuf0 + kQBytes + kRopeBytes + 4 * lane));
+  const float x = __uint_as_float(uint32_t(kx16) << 16);
+  const float y = __uint_as_float(uint32_t(ky16) << 16);
+  const float c = __uint_as_float(cb), sn = __uint_as_float(sb);
+  const float ks = p.k_scale[layer], vs = p.v_scale[layer];
+  const float kr_inv = exact_reciprocal(ks), vr_inv = exact_reciprocal(vs);
+  const float xr = __fsub_rn(__fmul_rn(x, c), __fmul_rn(y, sn));
+  const float yr = __fadd_rn(__fmul_rn(y, c), __fmul_rn(x, sn));
+  return f32x2_to_e4m3x2(div_scale(xr, ks, kr_inv), div_scale(yr, ks, kr_inv)) |
+         (f32x2_to_e4m3x2(div_scale(bf16lo_to_f32(vw), vs, vr_inv),
+                          div_scale(bf16hi_to_f32(vw), vs, vr_inv))
+          << 16);
+}
+
+template <bool kPackedK>
+__device__ __noinline__ void fused_patch(const AttnParams& p, int32_t ap_slot, uint32_t ap_codes,
+                                         int layer, int kvh, int lane, uint32_t Ks, uint32_t Vs,
+                                         int tl) {
+  if (ap_slot < 0 || int64_t(ap_slot) >= int64_t(p.nb) * p.B) {
+    if (lane == 0) set_error(GK_DEVERR_SLOT);
+    return;
+  }
+  const int pbi = fdiv(ap_slot, p.fd_b);
+  const int64_t pb = pbi;
+  const int t = ap_slot - pbi * p.B;
+  constexpr int es = kPackedK ? 2 : 1;  // byte step between channels of a K row
+  uint8_t* kdst =
+      const_cast<uint8_t*>(p.kb[layer >> 1]) +
+      (kPackedK ? ((pb * p.Hkv + kvh) * (p.B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1)
+                : ((pb * p.Hkv + kvh) * p.B + t) * kHeadDim);
+  kdst[es * lane] = uint8_t(ap_codes & 0xffu);
+  kdst[es * (lane + 32)] = uint8_t((ap_codes >> 8) & 0xffu);
+  uint8_t* vdst = const_cast<uint8_t*>(p.vb[layer >> 1]) + ((pb * p.Hkv + kvh) * p.B + t) * kHeadDim;
+  reinterpret_cast<uint16_t*>(vdst)[lane] = uint16_t(ap_codes >> 16);
+  const uint32_t kp = kPackedK ? Ks + (tl >> 1) * (2 * kHeadDim) + (tl & 1) : Ks + tl * kHeadDim;
+  const uint16_t k0 = uint16_t(ap_codes & 0xffu), k1 = uint16_t((ap_codes >> 8) & 0xffu);
+  asm volatile("st.shared.u8 [%0], %1;" ::"r"(kp + es * lane), "h"(k0) : "memory");
+  asm volatile("st.shared.u8 [%0], %1;" ::"r"(kp + es * (lane + 32)), "h"(k1) : "memory");
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(Vs + tl * kHeadDim + 2 * lane),
+               "h"(uint16_t(ap_codes >> 16))
+               : "memory");
 }
 
 // kMma = true: QK^T and PV on the tensor cores (the product path).
@@ -510,7 +567,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   bool tn_ready = false;
   int32_t tbl_next = 0;
   int tbl_next_base = 0;
-  int32_t upd_next = 0;  // fused step: update slot of the next unit's row and layer
   // lane l: entry l of the table chunk starting at the unit's first block
   auto load_tbl = [&](int4 e, int& base) -> int32_t {
     const bool swa = ((e.w >> 30) & 1) != 0;
@@ -533,16 +589,15 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   int32_t tbl = 0;
   bool failed = false;
   bool q_free = true;  // the q buffer may take the next unit's q
-  bool pu_appends = false;  // fused step: the producer's unit carries the new token
 
   // lane 0: copy the producer unit's q (8 heads) and its row's cos/sin rows
-  auto issue_unit_head = [&](uint32_t bar) {
+  auto issue_unit_head = [&](uint32_t bar, bool appends) {
     const uint16_t* qsrc =
         p.q + ((int64_t(pu_layer) * p.Bt + pu_b) * p.Hq + int64_t(pu_kvh) * kGroup) * kHeadDim;
     bulk_g2s(qbuf0, qsrc, kQBytes, bar);
     bulk_g2s(qbuf0 + kQBytes, p.cosb + int64_t(pu_b) * (kHeadDim / 2), kRopeBytes, bar);
     bulk_g2s(qbuf0 + kQBytes + kRopeBytes, p.sinb + int64_t(pu_b) * (kHeadDim / 2), kRopeBytes, bar);
-    if (kFused && pu_appends) {
+    if (kFused && appends) {
       const int64_t row = (int64_t(pu_layer) * p.Bt + pu_b) * p.Hkv + pu_kvh;
       bulk_g2s(qbuf0 + kUnitHeadBytes, p.k_new + row * kHeadDim, kHeadDim * 2, bar);
       bulk_g2s(qbuf0 + kUnitHeadBytes + kHeadDim * 2, p.v_new + row * kHeadDim, kHeadDim * 2, bar);
@@ -558,18 +613,12 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       if (u >= nU + nZ) return false;
       int32_t tcur = 0;
       int tcur_base = 0;
-      int32_t ucur = 0;
       if (u < nU) {
         if (tn_ready) {
           tcur = tbl_next;
           tcur_base = tbl_next_base;
-          ucur = upd_next;
         } else {
           tcur = load_tbl(e, tcur_base);
-          if constexpr (kFused) {
-            const bool swa_u = ((e.w >> 30) & 1) != 0;
-            ucur = swa_u ? __ldg(p.upd_swa + e.x) : __ldg(p.upd_full + e.x);
-          }
         }
       }
       if (lane == 0) u_after = atomicAdd(p.queue, 1);
@@ -583,7 +632,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         continue;
       }
       decode_unit(p, u, e, planes, d);
-      d.slot = ucur;
       tbl = tcur;
       tbl_base = tcur_base;
       return true;
@@ -592,6 +640,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
 
   auto issue_next = [&]() -> bool {
     if (exhausted) return false;
+    bool appends = false;  // fused step: the unit started here carries the new token
     if (pk == pu_n_st) {
       if (!q_free) return false;  // the consumer has not read the buffered q yet
       UnitDesc d;
@@ -600,6 +649,12 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         return false;
       }
       if (lane == 0) ws.fifo[f_tail % kFifo] = d;
+      if constexpr (kFused) {
+        appends = d.s == d.ns - 1;
+        if (appends && lane == 0)
+          cp_async4(smem_u32(&ws.ap_slot[f_tail % kFifo]),
+                    d.kind == 2 ? p.upd_swa + d.b : p.upd_full + d.b);
+      }
       __syncwarp();
       ++f_tail;
       pk = 0;
@@ -622,17 +677,12 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         ws.pu_base[1] = p.vb[d.layer >> 1] + head;
       }
       q_free = false;
-      pu_appends = kFused && d.s == d.ns - 1;
     } else if (!tn_ready && u_next < nU) {
       tbl_next = load_tbl(e_next, tbl_next_base);
-      if constexpr (kFused) {
-        const bool swa_next = ((e_next.w >> 30) & 1) != 0;
-        upd_next = swa_next ? __ldg(p.upd_swa + e_next.x) : __ldg(p.upd_full + e_next.x);
-      }
       tn_ready = true;
     }
     const uint32_t head_bytes =
-        pk == 0 ? kUnitHeadBytes + ((kFused && pu_appends) ? kNewKvBytes : 0u) : 0u;
+        pk == 0 ? kUnitHeadBytes + ((kFused && appends) ? kNewKvBytes : 0u) : 0u;
     const uint32_t dst = ring0 + p_slot * kStageBytes;
     const uint32_t bar = bar0 + 8 * p_slot;
     const bool two = p.B < kStageTok;  // 16-token blocks: two per stage
@@ -665,7 +715,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       if (lane == 0) {
         const int64_t off = int64_t(pb0) * blk_bytes + pu_off * kHeadDim + lo_b;
         mbar_arrive_expect_tx(bar, 2 * kbytes + head_bytes);
-        if (head_bytes) issue_unit_head(bar);
+        if (head_bytes) issue_unit_head(bar, appends);
         bulk_g2s(dst + lo_b, ws.pu_base[0] + off, kbytes, bar);
         bulk_g2s(dst + kStageKBytes + lo_b, ws.pu_base[1] + off, kbytes, bar);
       }
@@ -684,7 +734,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       if (lane == 0) {
         const uint32_t half = uint32_t(p.B) * kHeadDim;
         mbar_arrive_expect_tx(bar, (has1 ? 4 * half : 2 * half) + head_bytes);
-        if (head_bytes) issue_unit_head(bar);
+        if (head_bytes) issue_unit_head(bar, appends);
         const int64_t o0 = int64_t(pb0) * blk_bytes;
         bulk_g2s(dst, ws.pu_base[0] + o0, half, bar);
         bulk_g2s(dst + kStageKBytes, ws.pu_base[1] + o0, half, bar);
@@ -746,6 +796,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       cd.t_end = CU.t_end;
       cd.st_begin = CU.st_begin;
       cd.n_st = CU.n_st;
+      if constexpr (kFused) {
+        // the new token's codes, kept to the unit's last stage
+        if (CU.s == CU.ns - 1) ws.apbuf[lane] = fused_codes(p, qbuf0, CU.layer, lane);
+      }
       // ---- unit prologue: rotated q for head (kvh*8 + g), channels 16qd..16qd+15
       const uint32_t qrow = qbuf0 + g * (kHeadDim * 2);
       const uint4 x0 = lds128(qrow + 32 * qd);
@@ -763,34 +817,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         const uint4 s4 = lds128(sp + 16 * k);
         cw[4 * k] = c4.x; cw[4 * k + 1] = c4.y; cw[4 * k + 2] = c4.z; cw[4 * k + 3] = c4.w;
         sw[4 * k] = s4.x; sw[4 * k + 1] = s4.y; sw[4 * k + 2] = s4.z; sw[4 * k + 3] = s4.w;
-      }
-      if constexpr (kFused) {
-        if (CU.s == CU.ns - 1) {
-          // the same arithmetic as gk_kv_append, from the rows the head copy brought
-          const uint32_t kr = qbuf0 + kUnitHeadBytes;
-          uint16_t kx16, ky16;
-          asm volatile("ld.shared.u16 %0, [%1];" : "=h"(kx16) : "r"(kr + 2 * lane));
-          asm volatile("ld.shared.u16 %0, [%1];" : "=h"(ky16) : "r"(kr + 2 * (lane + 32)));
-          uint32_t vw, cb, sb;
-          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(vw) : "r"(kr + kHeadDim * 2 + 4 * lane));
-          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(cb) : "r"(qbuf0 + kQBytes + 4 * lane));
-          asm volatile("ld.shared.u32 %0, [%1];"
-                       : "=r"(sb)
-                       : "r"(qbuf0 + kQBytes + kRopeBytes + 4 * lane));
-          const float x = __uint_as_float(uint32_t(kx16) << 16);
-          const float y = __uint_as_float(uint32_t(ky16) << 16);
-          const float c = __uint_as_float(cb), sn = __uint_as_float(sb);
-          const float ks = p.k_scale[CU.layer], vs = p.v_scale[CU.layer];
-          const float kr_inv = exact_reciprocal(ks), vr_inv = exact_reciprocal(vs);
-          const float xr = __fsub_rn(__fmul_rn(x, c), __fmul_rn(y, sn));
-          const float yr = __fadd_rn(__fmul_rn(y, c), __fmul_rn(x, sn));
-          // k codes in the low half, v codes in the high half, kept to the last stage
-          ws.apbuf[lane] =
-              f32x2_to_e4m3x2(div_scale(xr, ks, kr_inv), div_scale(yr, ks, kr_inv)) |
-              (f32x2_to_e4m3x2(div_scale(bf16lo_to_f32(vw), vs, vr_inv),
-                               div_scale(bf16hi_to_f32(vw), vs, vr_inv))
-               << 16);
-        }
       }
       __syncwarp();
       q_free = true;
@@ -857,34 +883,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       if (k_in_unit == cd.n_st - 1 && CU.s == CU.ns - 1) {
         // the new token is the last key of the unit: store its codes to the
         // cache and into the staged copy (which holds the bytes from before)
-        const int32_t ap_slot = CU.slot;
-        const uint32_t ap_codes = ws.apbuf[lane];
-        if (ap_slot < 0 || int64_t(ap_slot) >= int64_t(p.nb) * p.B) {
-          if (lane == 0) set_error(GK_DEVERR_SLOT);
-        } else {
-          const int pbi = fdiv(ap_slot, p.fd_b);
-          const int64_t pb = pbi;
-          const int t = ap_slot - pbi * p.B;
-          constexpr int es = kPackedK ? 2 : 1;  // byte step between channels of a K row
-          uint8_t* kdst =
-              const_cast<uint8_t*>(p.kb[CU.layer >> 1]) +
-              (kPackedK ? ((pb * p.Hkv + CU.kvh) * (p.B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1)
-                        : ((pb * p.Hkv + CU.kvh) * p.B + t) * kHeadDim);
-          kdst[es * lane] = uint8_t(ap_codes & 0xffu);
-          kdst[es * (lane + 32)] = uint8_t((ap_codes >> 8) & 0xffu);
-          uint8_t* vdst = const_cast<uint8_t*>(p.vb[CU.layer >> 1]) +
-                          ((pb * p.Hkv + CU.kvh) * p.B + t) * kHeadDim;
-          reinterpret_cast<uint16_t*>(vdst)[lane] = uint16_t(ap_codes >> 16);
-          const int tl = cd.t_end - 1 - tok0;
-          const uint32_t kp =
-              kPackedK ? Ks + (tl >> 1) * (2 * kHeadDim) + (tl & 1) : Ks + tl * kHeadDim;
-          const uint16_t k0 = uint16_t(ap_codes & 0xffu), k1 = uint16_t((ap_codes >> 8) & 0xffu);
-          asm volatile("st.shared.u8 [%0], %1;" ::"r"(kp + es * lane), "h"(k0) : "memory");
-          asm volatile("st.shared.u8 [%0], %1;" ::"r"(kp + es * (lane + 32)), "h"(k1) : "memory");
-          asm volatile("st.shared.u16 [%0], %1;" ::"r"(Vs + tl * kHeadDim + 2 * lane),
-                       "h"(uint16_t(ap_codes >> 16))
-                       : "memory");
-        }
+        if (lane == 0) cp_async_wait_all();
+        __syncwarp();
+        fused_patch<kPackedK>(p, ws.ap_slot[f_head % kFifo], ws.apbuf[lane], CU.layer, CU.kvh,
+                              lane, Ks, Vs, cd.t_end - 1 - tok0);
         __syncwarp();
       }
     }
