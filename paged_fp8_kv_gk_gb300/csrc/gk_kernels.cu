@@ -424,6 +424,7 @@ struct alignas(128) WarpSmemT {
   // to key hi of their 32-key stages (its range rounded out to 8): lo | hi << 8
   int pu_trim;
   int32_t ap_slot[kFifo];  // fused step: update slot of each FIFO unit (copied asynchronously)
+  int4 e_next;             // work descriptor of the claimed unit (copied asynchronously)
   UnitDesc fifo[kFifo];
 };
 static_assert(sizeof(WarpSmemT<true>) % 128 == 0 && sizeof(WarpSmemT<false>) % 128 == 0,
@@ -448,9 +449,8 @@ __device__ __forceinline__ void zero_row(const AttnParams& p, int layer, int b, 
 }
 
 // Unit u covers plane u % planes of work entry e = u / planes.
-__device__ __forceinline__ void decode_unit(const AttnParams& p, int u, int4 e, int planes,
-                                            UnitDesc& d) {
-  const int pl = u - fdiv(u, p.fd_planes) * planes;
+__device__ __forceinline__ void decode_unit(const AttnParams& p, int u, int4 e, UnitDesc& d) {
+  const int pl = u - fdiv(u, p.fd_planes) * int(p.fd_planes.d);
   const int j = fdiv(pl, p.fd_hkv);
   const bool swa = ((e.w >> 30) & 1) != 0;
   d.kind = swa ? 2 : 1;
@@ -551,8 +551,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
 
   // the planner grid (launched just before) must be complete from here on
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int nU = p.hdr[kHdrNUnits], nZ = p.hdr[kHdrNZero];
-  const int planes = (p.NL >> 1) * p.Hkv;
+  const int nU = p.hdr[kHdrNUnits];
+  const int nAll = nU + p.hdr[kHdrNZero];  // units with a descriptor, then zero-fill units
 
   // ------------------------------------------------ scheduler pipeline
   // Each warp holds one claimed unit ahead of the one it streams: its
@@ -563,7 +563,19 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     u_next = atomicAdd(p.queue, 1);
   }
   u_next = __shfl_sync(kFull, u_next, 0);
-  int4 e_next = u_next < nU ? p.edesc[fdiv(u_next, p.fd_planes)] : make_int4(0, 0, 0, 0);
+  // the claimed unit's descriptor travels into shared memory by cp.async (no
+  // registers held while it is in flight); read_desc waits for it
+  auto claim_desc = [&](int u) {
+    if (lane == 0 && u < nU) cp_async16(smem_u32(&ws.e_next), p.edesc + fdiv(u, p.fd_planes));
+  };
+  auto read_desc = [&]() -> int4 {
+    if (lane == 0) cp_async_wait_all();
+    __syncwarp();
+    const int4 e = ws.e_next;
+    __syncwarp();
+    return e;
+  };
+  claim_desc(u_next);
   bool tn_ready = false;
   int32_t tbl_next = 0;
   int tbl_next_base = 0;
@@ -581,7 +593,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   int prod = 0, cons = 0;
   int f_head = 0, f_tail = 0;
   bool exhausted = false;
-  int pk = 0, pu_n_st = 0, pu_layer = 0, pu_b = 0, pu_kvh = 0, pu_t_end = 0, pu_kind = 0;
+  // (the producer unit's other fields are read from its FIFO entry, the last one pushed)
+  int pk = 0, pu_n_st = 0;
   // the producer's unit, advanced stage by stage: block (row index) and key
   // offset of the next stage (its K/V bases are in ws.pu_base)
   int pu_blk = 0, pu_off = 0, p_slot = 0;
@@ -591,14 +604,14 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   bool q_free = true;  // the q buffer may take the next unit's q
 
   // lane 0: copy the producer unit's q (8 heads) and its row's cos/sin rows
-  auto issue_unit_head = [&](uint32_t bar, bool appends) {
+  auto issue_unit_head = [&](uint32_t bar, bool appends, int layer, int b, int kvh) {
     const uint16_t* qsrc =
-        p.q + ((int64_t(pu_layer) * p.Bt + pu_b) * p.Hq + int64_t(pu_kvh) * kGroup) * kHeadDim;
+        p.q + ((int64_t(layer) * p.Bt + b) * p.Hq + int64_t(kvh) * kGroup) * kHeadDim;
     bulk_g2s(qbuf0, qsrc, kQBytes, bar);
-    bulk_g2s(qbuf0 + kQBytes, p.cosb + int64_t(pu_b) * (kHeadDim / 2), kRopeBytes, bar);
-    bulk_g2s(qbuf0 + kQBytes + kRopeBytes, p.sinb + int64_t(pu_b) * (kHeadDim / 2), kRopeBytes, bar);
+    bulk_g2s(qbuf0 + kQBytes, p.cosb + int64_t(b) * (kHeadDim / 2), kRopeBytes, bar);
+    bulk_g2s(qbuf0 + kQBytes + kRopeBytes, p.sinb + int64_t(b) * (kHeadDim / 2), kRopeBytes, bar);
     if (kFused && appends) {
-      const int64_t row = (int64_t(pu_layer) * p.Bt + pu_b) * p.Hkv + pu_kvh;
+      const int64_t row = (int64_t(layer) * p.Bt + b) * p.Hkv + kvh;
       bulk_g2s(qbuf0 + kUnitHeadBytes, p.k_new + row * kHeadDim, kHeadDim * 2, bar);
       bulk_g2s(qbuf0 + kUnitHeadBytes + kHeadDim * 2, p.v_new + row * kHeadDim, kHeadDim * 2, bar);
     }
@@ -609,8 +622,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   auto next_unit = [&](UnitDesc& d) -> bool {
     for (;;) {
       const int u = u_next;
-      const int4 e = e_next;
-      if (u >= nU + nZ) return false;
+      if (u >= nAll) return false;
+      const int4 e = u < nU ? read_desc() : make_int4(0, 0, 0, 0);
       int32_t tcur = 0;
       int tcur_base = 0;
       if (u < nU) {
@@ -623,7 +636,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       }
       if (lane == 0) u_after = atomicAdd(p.queue, 1);
       u_next = __shfl_sync(kFull, u_after, 0);
-      e_next = u_next < nU ? p.edesc[fdiv(u_next, p.fd_planes)] : make_int4(0, 0, 0, 0);
+      claim_desc(u_next);
       tn_ready = false;
       if (u >= nU) {
         const int v = u - nU;
@@ -631,7 +644,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         zero_row(p, v - zr * p.NL, p.zero_list[zr], lane);
         continue;
       }
-      decode_unit(p, u, e, planes, d);
+      decode_unit(p, u, e, d);
       tbl = tcur;
       tbl_base = tcur_base;
       return true;
@@ -641,6 +654,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   auto issue_next = [&]() -> bool {
     if (exhausted) return false;
     bool appends = false;  // fused step: the unit started here carries the new token
+    int h_layer = 0, h_b = 0, h_kvh = 0;  // the unit started here (for its head copy)
     if (pk == pu_n_st) {
       if (!q_free) return false;  // the consumer has not read the buffered q yet
       UnitDesc d;
@@ -659,11 +673,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       ++f_tail;
       pk = 0;
       pu_n_st = d.n_st;
-      pu_layer = d.layer;
-      pu_b = d.b;
-      pu_kvh = d.kvh;
-      pu_t_end = d.t_end;
-      pu_kind = d.kind;
+      h_layer = d.layer;
+      h_b = d.b;
+      h_kvh = d.kvh;
       {
         const int tok = d.st_begin * kStageTok;
         pu_blk = fdiv(tok, p.fd_b);
@@ -678,7 +690,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       }
       q_free = false;
     } else if (!tn_ready && u_next < nU) {
-      tbl_next = load_tbl(e_next, tbl_next_base);
+      tbl_next = load_tbl(read_desc(), tbl_next_base);
       tn_ready = true;
     }
     const uint32_t head_bytes =
@@ -686,10 +698,11 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     const uint32_t dst = ring0 + p_slot * kStageBytes;
     const uint32_t bar = bar0 + 8 * p_slot;
     const bool two = p.B < kStageTok;  // 16-token blocks: two per stage
-    const int row_len = pu_kind == 1 ? p.MBF : p.MBS;
     if (tbl_base < 0 || pu_blk + (two ? 1 : 0) >= tbl_base + 32) {
-      const int32_t* row = pu_kind == 1 ? p.bt_full + int64_t(pu_b) * p.MBF
-                                        : p.bt_swa + int64_t(pu_b) * p.MBS;
+      const UnitDesc& du = ws.fifo[(f_tail + kFifo - 1) % kFifo];
+      const int row_len = du.kind == 1 ? p.MBF : p.MBS;
+      const int32_t* row = du.kind == 1 ? p.bt_full + int64_t(du.b) * p.MBF
+                                        : p.bt_swa + int64_t(du.b) * p.MBS;
       tbl_base = pu_blk;
       const int idx = pu_blk + lane;
       tbl = idx < row_len ? row[idx] : 0;
@@ -715,7 +728,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       if (lane == 0) {
         const int64_t off = int64_t(pb0) * blk_bytes + pu_off * kHeadDim + lo_b;
         mbar_arrive_expect_tx(bar, 2 * kbytes + head_bytes);
-        if (head_bytes) issue_unit_head(bar, appends);
+        if (head_bytes) issue_unit_head(bar, appends, h_layer, h_b, h_kvh);
         bulk_g2s(dst + lo_b, ws.pu_base[0] + off, kbytes, bar);
         bulk_g2s(dst + kStageKBytes + lo_b, ws.pu_base[1] + off, kbytes, bar);
       }
@@ -726,7 +739,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       }
     } else {
       int32_t pb1 = __shfl_sync(kFull, tbl, min(pu_blk + 1 - tbl_base, 31));
-      const bool has1 = (pu_blk + 1) * p.B < pu_t_end;
+      const UnitDesc& du = ws.fifo[(f_tail + kFifo - 1) % kFifo];
+      const int row_len = du.kind == 1 ? p.MBF : p.MBS;
+      const bool has1 = (pu_blk + 1) * p.B < du.t_end;
       if (has1 && (pu_blk + 1 >= row_len || uint32_t(pb1) >= uint32_t(p.nb))) {
         if (lane == 0) set_error(GK_DEVERR_BLOCK);
         pb1 = 0;
@@ -734,7 +749,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       if (lane == 0) {
         const uint32_t half = uint32_t(p.B) * kHeadDim;
         mbar_arrive_expect_tx(bar, (has1 ? 4 * half : 2 * half) + head_bytes);
-        if (head_bytes) issue_unit_head(bar, appends);
+        if (head_bytes) issue_unit_head(bar, appends, h_layer, h_b, h_kvh);
         const int64_t o0 = int64_t(pb0) * blk_bytes;
         bulk_g2s(dst, ws.pu_base[0] + o0, half, bar);
         bulk_g2s(dst + kStageKBytes, ws.pu_base[1] + o0, half, bar);
@@ -1192,15 +1207,17 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         ro0[1] = make_float4(o[2][0], o[2][2], o[3][0], o[3][2]);
         ro1[0] = make_float4(o[0][1], o[0][3], o[1][1], o[1][3]);
         ro1[1] = make_float4(o[2][1], o[2][3], o[3][1], o[3][3]);
-        __threadfence();
+        // the warp barrier orders every lane's partial stores before lane 0's
+        // release; the last arriver's acquire (then the barrier) orders its
+        // reads of the other splits' partials after their releases
         __syncwarp();
         int old = 0;
         int32_t* ticket = p.tickets + (int64_t(j) * p.Bt + CU.b) * p.Hkv + CU.kvh;
-        if (lane == 0) old = atomicAdd(ticket, 1);
+        if (lane == 0) old = atom_add_acq_rel_gpu(ticket, 1);
         old = __shfl_sync(kFull, old, 0);
         if (old == CU.ns - 1) {
           // last split to finish: merge all of this row's partials in split order
-          __threadfence();
+          __syncwarp();
           const float* base = p.partials + (plane * cap + p.part_base[CU.b]) * kPartialFloats;
           float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
           float a0[8], a1[8];
