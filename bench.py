@@ -103,6 +103,43 @@ def recorded_traffic(workload: str):
     return e.get("dram_bytes_per_launch")
 
 
+def record_traffic(workload: str, csv_path: str, out_path: str = None) -> dict:
+    """Average DRAM bytes per attention launch from an ncu launch list (the
+    `--metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum
+    --csv` output of a run of this bench on `workload`) into
+    profiles/attn_traffic.json, stamped with the current kernel source hash."""
+    import csv
+    vals = {}
+    with open(csv_path) as f:
+        rows = [r for r in csv.reader(f) if len(r) > 5]
+    hdr = {k: i for i, k in enumerate(rows[0])}
+    for r in rows[1:]:
+        if "attn_kernel" not in r[hdr["Kernel Name"]]:
+            continue
+        v = float(r[hdr["Metric Value"]].replace(",", ""))
+        vals.setdefault(r[hdr["Metric Name"]], []).append(v)
+    rd = statistics.fmean(vals["dram__bytes_read.sum"])
+    wr = statistics.fmean(vals["dram__bytes_write.sum"])
+    entry = {"kernel_src_sha": attn_source_hash(), "dram_bytes_per_launch": int(rd + wr),
+             "dram_read_bytes": int(rd), "dram_write_bytes": int(wr),
+             "launches_averaged": len(vals["dram__bytes_read.sum"]),
+             "avg_launch_ns_under_ncu": round(statistics.fmean(vals["gpu__time_duration.sum"]), 1),
+             "command": "ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,"
+                        "dram__bytes_write.sum --clock-control none -k regex:\"attn_kernel|"
+                        "plan_kernel|kv_append_kernel\" --csv --log-file launches.csv python "
+                        f"bench.py --workload {workload} --steps 3 --warmup 3 --no-cpu-baseline"}
+    p = out_path or os.path.join(ROOT, "profiles", "attn_traffic.json")
+    d = {}
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+    d[workload] = entry
+    with open(p, "w") as f:
+        json.dump(d, f, indent=1)
+        f.write("\n")
+    return entry
+
+
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons; only samples whose
     timestamp falls inside the timed region (mark_begin .. mark_end) count."""
@@ -651,9 +688,15 @@ def main(argv=None):
                     help="K through the packed view (the page's layout) or unpacked like V")
     ap.add_argument("--kv-form", choices=["per_group", "stacked"], default="per_group",
                     help="per-group K/V buffers or stacked K_cache/V_cache")
+    ap.add_argument("--record-traffic", metavar="LAUNCHES_CSV", default=None,
+                    help="store the attention kernel's DRAM bytes per launch from an ncu launch "
+                         "list of --workload into profiles/attn_traffic.json, then exit")
     ap.add_argument("--ws-min", action="store_true",
                     help="use the minimum attention workspace (no split-KV chunks)")
     args = ap.parse_args(argv)
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args.workload or DEFAULT_WORKLOAD, args.record_traffic)))
+        return
     if args.workload is None:
         args.workload = "di_ingest_b16" if args.op == "ingest" else DEFAULT_WORKLOAD
     if args.op == "ingest":

@@ -837,15 +837,16 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       q_free = true;
       const float sgn = qd < 2 ? -1.f : 1.f;
       // logits in log2 units: q'.k * k_scale / sqrt(D) * log2(e), folded into q
+      // (for the MMA path together with the power-of-two normalisation below)
       const float ck = p.k_scale[CU.layer] * (0.125f * 1.4426950408889634f);
-      float r[16];
+      float r[16];  // rotated q, before the ck scaling
       float amax = 0.f;
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
         const float c0 = __uint_as_float(cw[2 * w]), c1 = __uint_as_float(cw[2 * w + 1]);
         const float s0 = __uint_as_float(sw[2 * w]), s1 = __uint_as_float(sw[2 * w + 1]);
-        r[2 * w] = (bf16lo_to_f32(xw[w]) * c0 + sgn * bf16lo_to_f32(yw[w]) * s0) * ck;
-        r[2 * w + 1] = (bf16hi_to_f32(xw[w]) * c1 + sgn * bf16hi_to_f32(yw[w]) * s1) * ck;
+        r[2 * w] = bf16lo_to_f32(xw[w]) * c0 + sgn * bf16lo_to_f32(yw[w]) * s0;
+        r[2 * w + 1] = bf16hi_to_f32(xw[w]) * c1 + sgn * bf16hi_to_f32(yw[w]) * s1;
         amax = fmaxf(amax, fmaxf(fabsf(r[2 * w]), fabsf(r[2 * w + 1])));
       }
       if constexpr (!kMma) {
@@ -854,7 +855,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           reinterpret_cast<float4*>(qrow_f)[k] =
-              make_float4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]);
+              make_float4(r[4 * k] * ck, r[4 * k + 1] * ck, r[4 * k + 2] * ck, r[4 * k + 3] * ck);
         __syncwarp();
 #pragma unroll
         for (int h = 0; h < kGroup; ++h) {
@@ -865,15 +866,16 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         si0 = si1 = 1.f;
       }
       amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2)) * ck;
       // power-of-two normalisation of the head so that max |q'| < 2^14 in f16
       int ex = int((__float_as_uint(amax) >> 23) & 0xffu) - 127;
       ex = amax > 0.f ? min(max(ex, -100), 100) : 13;
       const float f = __uint_as_float(uint32_t(127 + 13 - ex) << 23);
       const float finv = __uint_as_float(uint32_t(127 - 13 + ex) << 23);
+      const float fck = f * ck;  // fl(x * fck) == fl(x * ck) * f: f is a power of two
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
-        const float a = r[2 * w] * f, b = r[2 * w + 1] * f;
+        const float a = r[2 * w] * fck, b = r[2 * w + 1] * fck;
         qhi[w] = f32x2_to_f16x2(a, b);
         const float2 h = f16x2_to_f32x2(qhi[w]);
         qlo[w] = f32x2_to_f16x2(a - h.x, b - h.y);  // residual is exact in fp32

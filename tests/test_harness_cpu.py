@@ -44,3 +44,29 @@ def test_appended_codes_helper_equals_whole_buffer_append(name):
             pb, t = divmod(int(upd[b]), B)
             assert np.array_equal(kc[i, b], kview[pb, :, t // 2, :, t % 2])
             assert np.array_equal(vc[i, b], vview[pb, :, t, :])
+
+
+def test_bench_records_traffic_from_an_ncu_launch_list(tmp_path):
+    """bench.py --record-traffic: the attention kernel's launches are averaged
+    (other kernels ignored) and stamped with the current source hash."""
+    import bench
+    csv_path = tmp_path / "launches.csv"
+    hdr = '"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",' \
+          '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",' \
+          '"Metric Value"\n'
+    rows = []
+    for i, (k, rd, wr, t) in enumerate([("void attn_kernel<1, 0, 1>(AttnParams)", 100, 10, 5),
+                                        ("plan_kernel(PlanParams)", 7, 0, 1),
+                                        ("void attn_kernel<1, 0, 1>(AttnParams)", 300, 30, 7)]):
+        for m, v in (("dram__bytes_read.sum", rd), ("dram__bytes_write.sum", wr),
+                     ("gpu__time_duration.sum", t)):
+            rows.append(f'"{i}","1","python","h","{k}","1","7","(128, 1, 1)","(608, 1, 1)","0",'
+                        f'"10.3","Command line profiler metrics","{m}","byte","{v:,}"\n')
+    csv_path.write_text(hdr + "".join(rows))
+    out = tmp_path / "traffic.json"
+    e = bench.record_traffic("gptoss_b64", str(csv_path), str(out))
+    assert e["dram_read_bytes"] == 200 and e["dram_write_bytes"] == 20
+    assert e["dram_bytes_per_launch"] == 220 and e["launches_averaged"] == 2
+    assert e["kernel_src_sha"] == bench.attn_source_hash()
+    import json
+    assert json.loads(out.read_text())["gptoss_b64"]["dram_bytes_per_launch"] == 220
