@@ -1163,7 +1163,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       const int64_t out_row =
           ((int64_t(CU.layer) * p.Bt + CU.b) * p.Hq + CU.kvh * kGroup + 2 * qd) * kHeadDim + 8 * g;
       if (CU.ns == 1) {
-        const float i0 = vscale / l0, i1 = vscale / l1;
+        const float i0 = vscale * __frcp_rn(l0), i1 = vscale * __frcp_rn(l1);
         float r0[8], r1[8];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
@@ -1248,7 +1248,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
               a1[c] = a1[c] * c1 + q1[c] * w1;
             }
           }
-          const float i0 = vscale / L0, i1 = vscale / L1;
+          const float i0 = vscale * __frcp_rn(L0), i1 = vscale * __frcp_rn(L1);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             a0[c] *= i0;
