@@ -439,6 +439,21 @@ def run_gk(args):
             append()
             attention()
 
+    if args.graph:
+        # the whole step captured once (on a side stream: the legacy default
+        # stream cannot be captured) and replayed on the timing stream
+        one_step()                       # device setup happens outside the capture
+        torch.cuda.synchronize(dev)
+        cap = torch.cuda.Stream(dev)
+        sh = cap.cuda_stream
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            one_step()
+        sh = stream.cuda_stream
+
+        def one_step():
+            graph.replay()
+
     K, W = args.steps, args.warmup
     for _ in range(W):
         one_step()
@@ -532,7 +547,7 @@ def run_gk(args):
         "e2e": {"value": round(e2e_units / (e2e_ms / 1e3), 1), "unit": UNIT,
                 "ms_per_step": round(e2e_ms / K, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "step_form": args.step,
+        "step_form": args.step + (" (CUDA graph)" if args.graph else ""),
         "gpu_launches": (2 if args.step == "fused" else 3) * K,  # per timed step
         "clocks": clk,
     }
@@ -688,6 +703,8 @@ def main(argv=None):
                     help="K through the packed view (the page's layout) or unpacked like V")
     ap.add_argument("--kv-form", choices=["per_group", "stacked"], default="per_group",
                     help="per-group K/V buffers or stacked K_cache/V_cache")
+    ap.add_argument("--graph", action="store_true",
+                    help="time the step as one captured CUDA graph replayed per step")
     ap.add_argument("--record-traffic", metavar="LAUNCHES_CSV", default=None,
                     help="store the attention kernel's DRAM bytes per launch from an ncu launch "
                          "list of --workload into profiles/attn_traffic.json, then exit")
