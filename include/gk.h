@@ -27,6 +27,10 @@
  *   - `stream` is a cudaStream_t passed as void*.  Calls are asynchronous and
  *     stream-ordered: a call returns after validating its arguments and
  *     enqueueing its kernels.  NULL means the legacy default stream.
+ *   - Calls may be captured into a CUDA graph and replayed (the step's
+ *     launches are chained by programmatic dependent launch, which capture
+ *     keeps).  The first call on a device sets kernel attributes and caches
+ *     device properties: make it before any capture.
  *   - Errors: every entry point returns a gk_status and never aborts, traps or
  *     prints.  Argument checks run on the host before anything is enqueued; a
  *     failed check enqueues nothing.  Launch failures map to GK_ERR_CUDA.
