@@ -78,9 +78,9 @@ def lib():
             L.ora_kv_append.restype = ctypes.c_int
             L.ora_kv_append.argtypes = [ctypes.POINTER(Shape)] + [vp] * 11
             L.ora_decode_attn_stack.restype = ctypes.c_int
-            L.ora_decode_attn_stack.argtypes = [ctypes.POINTER(Shape)] + [vp] * 13
+            L.ora_decode_attn_stack.argtypes = [ctypes.POINTER(Shape)] + [vp] * 14
             L.ora_attn_one_ex.restype = ctypes.c_int
-            L.ora_attn_one_ex.argtypes = ([ctypes.POINTER(Shape)] + [vp] * 12
+            L.ora_attn_one_ex.argtypes = ([ctypes.POINTER(Shape)] + [vp] * 13
                                           + [i32, i32, i32, i32, vp])
             L.ora_kv_regions.restype = i32
             L.ora_kv_regions.argtypes = [i32, vp, vp, vp]
@@ -186,8 +186,9 @@ def kv_append(shape: Shape, k_new, v_new, cos, sin, k_scale, v_scale, upd_full, 
 
 
 def decode_attn_stack(shape: Shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, sin, bt_full,
-                      bt_swa, pos, pos_w, active):
-    """Whole-stack decode attention in fp64; returns (out [NL,Bt,Hq,D] float64, status)."""
+                      bt_swa, pos, pos_w, active, sinks=None):
+    """Whole-stack decode attention in fp64; returns (out [NL,Bt,Hq,D] float64, status).
+    sinks: optional [NL, Hq] attention-sink logits (natural units)."""
     q = _c(q, np.uint16)
     k_bufs = [_c(a, np.uint8) for a in k_bufs]
     v_bufs = [_c(a, np.uint8) for a in v_bufs]
@@ -196,14 +197,15 @@ def decode_attn_stack(shape: Shape, q, k_bufs, v_bufs, k_scale, v_scale, cos, si
             _c(pos, np.int32), _c(pos_w, np.int32), _c(active, np.uint8)]
     out = np.zeros((shape.num_layers, shape.batch, shape.num_q_heads, shape.head_dim), np.float64)
     kp, vp_ = _ptr_array(k_bufs), _ptr_array(v_bufs)
+    sk = None if sinks is None else _c(np.asarray(sinks, np.float32), np.float32)
     st = lib().ora_decode_attn_stack(ctypes.byref(shape), _p(q), ctypes.cast(kp, ctypes.c_void_p),
                                      ctypes.cast(vp_, ctypes.c_void_p), *[_p(a) for a in args],
-                                     _p(out))
+                                     None if sk is None else _p(sk), _p(out))
     return out, st
 
 
 def attn_one(shape: Shape, q, kbuf, vbuf, k_scale, v_scale, cos, sin, bt_full, bt_swa, pos,
-             pos_w, active, layer, b, kvh, nsplit=1):
+             pos_w, active, layer, b, kvh, nsplit=1, sinks=None):
     """One (layer, sequence, kv head): returns (out [G, D] float64, status).
     ``kbuf``/``vbuf`` are the K and V halves of group buffer layer // 2."""
     G = shape.num_q_heads // shape.num_kv_heads
@@ -212,8 +214,9 @@ def attn_one(shape: Shape, q, kbuf, vbuf, k_scale, v_scale, cos, sin, bt_full, b
             _c(bt_full, np.int32), _c(bt_swa, np.int32), _c(pos, np.int32), _c(pos_w, np.int32),
             _c(active, np.uint8)]
     out = np.zeros((G, shape.head_dim), np.float64)
-    st = lib().ora_attn_one_ex(ctypes.byref(shape), *[_p(a) for a in arrs], layer, b, kvh,
-                               nsplit, _p(out))
+    sk = None if sinks is None else _c(np.asarray(sinks, np.float32), np.float32)
+    st = lib().ora_attn_one_ex(ctypes.byref(shape), *[_p(a) for a in arrs],
+                               None if sk is None else _p(sk), layer, b, kvh, nsplit, _p(out))
     return out, st
 
 

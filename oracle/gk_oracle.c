@@ -35,7 +35,10 @@
  *       one.  Positions are read in the trimmed table's frame: keys
  *       t in [max(0, pos_w - W + 1), pos_w].  Full layers: keys t in [0, pos].
  *   R6  GQA: q head h uses kv head h / (Hq/Hkv).  Softmax scale 1/sqrt(D).
- *       No attention-sink logits.  Inactive rows give zero output.
+ *       Inactive rows give zero output.  Optional attention sinks (GPT-OSS; not
+ *       on the pages): a per-layer, per-head logit sinks[i][h] (natural units)
+ *       joins the softmax denominator and carries no value:
+ *       out = sum_t e^(s_t) v_t / (sum_t e^(s_t) + e^(sink)).  NULL = none.
  *   R7  Layer i: even -> SWA (table bt_swa, index upd_swa, position pos_w),
  *       odd -> full (bt_full, upd_full, pos); KV buffer j = i / 2.  [GK Kernel contract]
  *
@@ -270,6 +273,7 @@ typedef struct {
     const int32_t *bt_full, *bt_swa; /* [Bt, MBF], [Bt, MBS] */
     const int32_t *pos, *pos_w;
     const uint8_t *active;
+    const float *sinks;       /* [NL, Hq] or NULL */
 } ora_attn_inputs;
 
 /* Key range [lo, hi] (inclusive, in the chosen table's frame) and table row. */
@@ -402,14 +406,20 @@ int ora_attn_one(const ora_shape *sh, const ora_attn_inputs *in, int32_t i, int3
             }
         }
     }
-    /* merge */
+    /* merge (a sink logit joins the denominator with no value) */
     for (int32_t g = 0; g < G; ++g) {
-        double M = -INFINITY, L = 0.0;
+        double M = -INFINITY, L = 0.0, sink = -INFINITY;
+        if (in->sinks)
+            sink = (double)in->sinks[(int64_t)i * sh->num_q_heads + (int64_t)kvh * G + g];
         for (int32_t s = 0; s < nsplit; ++s)
             if (ms[s * G + g] > M)
                 M = ms[s * G + g];
+        if (sink > M)
+            M = sink;
         for (int32_t s = 0; s < nsplit; ++s)
             L += exp(ms[s * G + g] - M) * ls[s * G + g];
+        if (in->sinks)
+            L += exp(sink - M);
         for (int32_t e = 0; e < D; ++e) {
             double acc = 0.0;
             for (int32_t s = 0; s < nsplit; ++s)
@@ -432,7 +442,8 @@ int ora_attn_one(const ora_shape *sh, const ora_attn_inputs *in, int32_t i, int3
 int ora_decode_attn_stack(const ora_shape *sh, const uint16_t *q, const uint8_t *const *k_bufs,
                           const uint8_t *const *v_bufs, const float *k_scale, const float *v_scale,
                           const float *cosb, const float *sinb, const int32_t *bt_full, const int32_t *bt_swa,
-                          const int32_t *pos, const int32_t *pos_w, const uint8_t *active, double *out)
+                          const int32_t *pos, const int32_t *pos_w, const uint8_t *active,
+                          const float *sinks, double *out)
 {
     const int32_t NL = sh->num_layers, Bt = sh->batch, Hq = sh->num_q_heads, Hkv = sh->num_kv_heads;
     const int32_t D = sh->head_dim, G = Hq / Hkv;
@@ -448,6 +459,7 @@ int ora_decode_attn_stack(const ora_shape *sh, const uint16_t *q, const uint8_t 
     in.pos = pos;
     in.pos_w = pos_w;
     in.active = active;
+    in.sinks = sinks;
     for (int32_t i = 0; i < NL; ++i) {
         in.kbuf = k_bufs[i / 2];
         in.vbuf = v_bufs[i / 2];
@@ -466,7 +478,8 @@ int ora_decode_attn_stack(const ora_shape *sh, const uint16_t *q, const uint8_t 
 int ora_attn_one_ex(const ora_shape *sh, const uint16_t *q, const uint8_t *kbuf, const uint8_t *vbuf,
                     const float *k_scale, const float *v_scale, const float *cosb, const float *sinb,
                     const int32_t *bt_full, const int32_t *bt_swa, const int32_t *pos, const int32_t *pos_w,
-                    const uint8_t *active, int32_t layer, int32_t b, int32_t kvh, int32_t nsplit, double *out)
+                    const uint8_t *active, const float *sinks, int32_t layer, int32_t b, int32_t kvh,
+                    int32_t nsplit, double *out)
 {
     ora_attn_inputs in;
     in.q = q;
@@ -481,6 +494,7 @@ int ora_attn_one_ex(const ora_shape *sh, const uint16_t *q, const uint8_t *kbuf,
     in.pos = pos;
     in.pos_w = pos_w;
     in.active = active;
+    in.sinks = sinks;
     return ora_attn_one(sh, &in, layer, b, kvh, nsplit, out);
 }
 

@@ -14,12 +14,12 @@ from . import attn_one, kv_append, make_shape
 
 
 def row_pair_from_pool(w, c, step_host: dict, kpool: np.ndarray, vpool: np.ndarray, j: int,
-                       b: int, kvhs=None, k_layout: int = 0) -> dict:
+                       b: int, kvhs=None, k_layout: int = 0, sinks=None) -> dict:
     """w, c: the workload and its control tensors (gk_inputs.Workload/Control).
     step_host: q, k_new, v_new as uint16 bf16 bit arrays.  kpool/vpool: bytes
     of row b's full blocks followed by its window blocks (K halves and V
     halves, each block Hkv*B*D bytes), from the cache before the append.
-    k_layout: 0 packed K view, 1 unpacked K.
+    k_layout: 0 packed K view, 1 unpacked K.  sinks: optional [NL, Hq] sink logits.
     Returns {(layer, kvh): [G, D] float64} for layers 2j and 2j+1."""
     B, Hkv, D, NL = w.block_size, w.num_kv_heads, w.head_dim, w.num_layers
     kvhs = range(Hkv) if kvhs is None else kvhs
@@ -55,7 +55,7 @@ def row_pair_from_pool(w, c, step_host: dict, kpool: np.ndarray, vpool: np.ndarr
         for kvh in kvhs:
             out, st = attn_one(sh, row(step_host["q"]), kmini, vmini, c.k_scale, c.v_scale,
                                c.cos[b:b + 1], c.sin[b:b + 1], bt_full, bt_swa, c.pos[b:b + 1],
-                               c.pos_w[b:b + 1], c.active[b:b + 1], layer, 0, kvh)
+                               c.pos_w[b:b + 1], c.active[b:b + 1], layer, 0, kvh, sinks=sinks)
             assert st == 0
             res[(layer, kvh)] = out
     return res
