@@ -56,7 +56,7 @@ def test_sink_scales_each_head_and_follows_exp(name):
     assert (a1 > 0).all() and (a1 < 1).all() and (a2 > a1).all()
     ratio = (1 / a1 - 1) / (1 / a2 - 1)
     d = s1.astype(np.float64) - s2.astype(np.float64)          # ~1.5 after the float32 rounding
-    np.testing.assert_allclose(ratio, np.exp(d)[:, None, :], rtol=1e-9)
+    np.testing.assert_allclose(ratio, np.broadcast_to(np.exp(d)[:, None, :], ratio.shape), rtol=1e-9)
 
 
 def test_split_combine_with_sinks():
