@@ -359,6 +359,18 @@ def make_landing(w: Workload, c: Control, cache: List[torch.Tensor]):
     return dst_region, dst_block, src
 
 
+def make_sinks(w: Workload, seed: int = 0) -> np.ndarray:
+    """Attention-sink logits fp32 [NL, Hq] (natural-log units, the scale of the
+    scores): N(0, 2), with every 7th head set to +12 (the sink dominates the
+    row) and every 11th to -30 (it vanishes)."""
+    rng = np.random.default_rng(w.seed * 7919 + 11 + seed)
+    s = rng.normal(0.0, 2.0, (w.num_layers, w.num_q_heads))
+    h = np.arange(w.num_q_heads)
+    s[:, h % 7 == 3] = 12.0
+    s[:, h % 11 == 5] = -30.0
+    return s.astype(np.float32)
+
+
 def kv_bytes_read(w: Workload, c: Control) -> int:
     """Algorithmic KV bytes one decode-attention step reads: each active row
     reads Hkv * D bytes of K and of V per key, L keys in full layers and

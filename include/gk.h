@@ -49,6 +49,8 @@
  *   pos, pos_w        int32 [Bt]                  absolute / window-frame position of the new token
  *   upd_full, upd_swa int32 [Bt]                  flat slot = block * B + offset
  *   active            uint8 [Bt]                  0 = row skipped (no write, zero output)
+ *   sinks             fp32  [NL, Hq] or NULL      optional attention-sink logits (see
+ *                                                 gk_decode_attn_stack)
  *   kv                the cache (gk_kv_cache): group buffer j's K and V halves, each
  *                     num_blocks * Hkv * B * D bytes (one FP8 byte per element):
  *                     K byte (pb, h, t, e) = ((pb*Hkv + h)*(B/2) + t/2)*(2D) + 2e + (t & 1)
@@ -168,6 +170,10 @@ size_t gk_attn_workspace_min_bytes(const gk_shape *shape);
  *   q' = RoPE(q[i,b,h,:], cos[b], sin[b]);  k_t = decode(K_{i/2}) * k_scale[i];
  *   v_t = decode(V_{i/2}) * v_scale[i];  s_t = q'.k_t / sqrt(D)
  *   out[i,b,h,:] = bf16_rne( sum_t softmax(s)_t v_t );  out_f32 (optional) gets the fp32 value.
+ * Attention sinks (GPT-OSS; not on the pages): when sinks is not NULL, the
+ * per-layer, per-head logit sinks[i*Hq + h] (natural-log units, like s_t)
+ * joins the softmax denominator and carries no value:
+ *   out = sum_t e^(s_t) v_t / (sum_t e^(s_t) + e^(sinks[i*Hq + h])).
  * Inactive rows get zeros.  The cache is read, never written: run gk_kv_append
  * first on the same stream when the new token must be attended to.
  * workspace: device memory, 256-byte aligned, ws_bytes >= gk_attn_workspace_min_bytes;
@@ -181,7 +187,7 @@ gk_status gk_decode_attn_stack(const gk_shape *shape, const void *q, const gk_kv
                                const float *k_scale, const float *v_scale,
                                const float *cos, const float *sin, const int32_t *bt_full,
                                const int32_t *bt_swa, const int32_t *pos, const int32_t *pos_w,
-                               const uint8_t *active, void *out, float *out_f32,
+                               const uint8_t *active, const float *sinks, void *out, float *out_f32,
                                void *workspace, size_t ws_bytes, void *stream);
 
 /*
@@ -205,7 +211,7 @@ gk_status gk_decode_step(const gk_shape *shape, const void *q, const void *k_new
                          const float *k_scale, const float *v_scale, const int32_t *upd_full,
                          const int32_t *upd_swa, const int32_t *bt_full, const int32_t *bt_swa,
                          const int32_t *pos, const int32_t *pos_w, const uint8_t *active,
-                         const gk_kv_cache *kv, void *out, float *out_f32,
+                         const float *sinks, const gk_kv_cache *kv, void *out, float *out_f32,
                          void *workspace, size_t ws_bytes, void *stream);
 
 /*
@@ -238,7 +244,8 @@ gk_status gk_decode_attn_stack_static(const gk_shape *shape, const void *q,
                                       const float *v_scale, const float *cos, const float *sin,
                                       const int32_t *bt_full, const int32_t *bt_swa,
                                       const int32_t *pos, const int32_t *pos_w,
-                                      const uint8_t *active, void *out, float *out_f32,
+                                      const uint8_t *active, const float *sinks, void *out,
+                                      float *out_f32,
                                       void *stream);
 
 /*
@@ -346,7 +353,7 @@ gk_status gk_di_blocks(int64_t num_tokens, int32_t block_size, int32_t window,
 /* Human-readable name of a status code (static string). */
 const char *gk_status_str(gk_status status);
 
-/* Library ABI version (2: the cache is passed as a gk_kv_cache). */
+/* Library ABI version (3: the cache is passed as a gk_kv_cache; optional sinks). */
 int32_t gk_abi_version(void);
 
 #ifdef __cplusplus

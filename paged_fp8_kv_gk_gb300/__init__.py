@@ -205,11 +205,11 @@ def lib(build_if_needed: bool = True) -> ctypes.CDLL:
             L.gk_attn_workspace_min_bytes.restype = sz
             L.gk_attn_workspace_min_bytes.argtypes = [sp]
             L.gk_decode_attn_stack.restype = ctypes.c_int
-            L.gk_decode_attn_stack.argtypes = [sp] + [vp] * 14 + [sz, vp]
+            L.gk_decode_attn_stack.argtypes = [sp] + [vp] * 15 + [sz, vp]
             L.gk_decode_step.restype = ctypes.c_int
-            L.gk_decode_step.argtypes = [sp] + [vp] * 18 + [sz, vp]
+            L.gk_decode_step.argtypes = [sp] + [vp] * 19 + [sz, vp]
             L.gk_decode_attn_stack_static.restype = ctypes.c_int
-            L.gk_decode_attn_stack_static.argtypes = [sp] + [vp] * 14
+            L.gk_decode_attn_stack_static.argtypes = [sp] + [vp] * 15
             L.gk_e4m3_quantize.restype = ctypes.c_int
             L.gk_e4m3_quantize.argtypes = [vp, ctypes.c_float, vp, i64, vp]
             L.gk_kv_budget.restype = ctypes.c_int
@@ -270,6 +270,17 @@ def _check(status: int, where: str):
         raise GkError(status, where)
 
 
+def _sinks(sinks, shape):
+    """Optional attention-sink logits: fp32 [NL, Hq] on the device, or None."""
+    import torch
+    if sinks is None:
+        return None
+    if sinks.numel() != shape.num_layers * shape.num_q_heads:
+        raise ValueError(f"sinks must hold num_layers * num_q_heads = "
+                         f"{shape.num_layers * shape.num_q_heads} values")
+    return _ptr(sinks, torch.float32, "sinks")
+
+
 def _as_shape(shape) -> Shape:
     if isinstance(shape, Shape):
         return shape
@@ -308,7 +319,7 @@ def gk_kv_append(shape, k_new, v_new, cos, sin, k_scale, v_scale, upd_full, upd_
 
 def gk_decode_attn_stack(shape, q, kv: KvCache, k_scale, v_scale, cos, sin, bt_full, bt_swa,
                          pos, pos_w, active, out, out_f32=None, workspace=None,
-                         stream=None) -> None:
+                         stream=None, sinks=None) -> None:
     import torch
     sh = _as_shape(shape)
     if workspace is None:
@@ -319,7 +330,7 @@ def gk_decode_attn_stack(shape, q, kv: KvCache, k_scale, v_scale, cos, sin, bt_f
         _ptr(cos, torch.float32, "cos"), _ptr(sin, torch.float32, "sin"),
         _ptr(bt_full, torch.int32, "bt_full"), _ptr(bt_swa, torch.int32, "bt_swa"),
         _ptr(pos, torch.int32, "pos"), _ptr(pos_w, torch.int32, "pos_w"),
-        _ptr(active, torch.uint8, "active"), _ptr(out, torch.bfloat16, "out"),
+        _ptr(active, torch.uint8, "active"), _sinks(sinks, sh), _ptr(out, torch.bfloat16, "out"),
         _ptr(out_f32, torch.float32, "out_f32", allow_none=True),
         _ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()), _stream(stream, q))
     _check(st, "gk_decode_attn_stack")
@@ -327,7 +338,7 @@ def gk_decode_attn_stack(shape, q, kv: KvCache, k_scale, v_scale, cos, sin, bt_f
 
 def gk_decode_step(shape, q, k_new, v_new, cos, sin, k_scale, v_scale, upd_full, upd_swa,
                    bt_full, bt_swa, pos, pos_w, active, kv: KvCache, out, out_f32=None,
-                   workspace=None, stream=None) -> None:
+                   workspace=None, stream=None, sinks=None) -> None:
     """gk_kv_append + gk_decode_attn_stack in one attention launch."""
     import torch
     sh = _as_shape(shape)
@@ -340,15 +351,16 @@ def gk_decode_step(shape, q, k_new, v_new, cos, sin, k_scale, v_scale, upd_full,
         _ptr(v_scale, torch.float32, "v_scale"), _ptr(upd_full, torch.int32, "upd_full"),
         _ptr(upd_swa, torch.int32, "upd_swa"), _ptr(bt_full, torch.int32, "bt_full"),
         _ptr(bt_swa, torch.int32, "bt_swa"), _ptr(pos, torch.int32, "pos"),
-        _ptr(pos_w, torch.int32, "pos_w"), _ptr(active, torch.uint8, "active"), _kv(kv, sh),
-        _ptr(out, torch.bfloat16, "out"), _ptr(out_f32, torch.float32, "out_f32", allow_none=True),
+        _ptr(pos_w, torch.int32, "pos_w"), _ptr(active, torch.uint8, "active"),
+        _sinks(sinks, sh), _kv(kv, sh), _ptr(out, torch.bfloat16, "out"),
+        _ptr(out_f32, torch.float32, "out_f32", allow_none=True),
         _ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()), _stream(stream, q))
     _check(st, "gk_decode_step")
 
 
 def gk_decode_attn_stack_static(shape, q, kv: KvCache, k_scale, v_scale, cos, sin, bt_full,
                                 bt_swa, pos, pos_w, active, out, out_f32=None,
-                                stream=None) -> None:
+                                stream=None, sinks=None) -> None:
     """gk_decode_attn_stack without a caller workspace, for callers that cannot
     allocate device memory: the library's own fixed scratch array
     (GK_STATIC_SCRATCH_BYTES per GPU) serves as the workspace.  Calls on one
@@ -361,7 +373,7 @@ def gk_decode_attn_stack_static(shape, q, kv: KvCache, k_scale, v_scale, cos, si
         _ptr(cos, torch.float32, "cos"), _ptr(sin, torch.float32, "sin"),
         _ptr(bt_full, torch.int32, "bt_full"), _ptr(bt_swa, torch.int32, "bt_swa"),
         _ptr(pos, torch.int32, "pos"), _ptr(pos_w, torch.int32, "pos_w"),
-        _ptr(active, torch.uint8, "active"), _ptr(out, torch.bfloat16, "out"),
+        _ptr(active, torch.uint8, "active"), _sinks(sinks, sh), _ptr(out, torch.bfloat16, "out"),
         _ptr(out_f32, torch.float32, "out_f32", allow_none=True), _stream(stream, q))
     _check(st, "gk_decode_attn_stack_static")
 

@@ -138,7 +138,7 @@ const char* gk_status_str(gk_status st) {
   return "GK_ERR_UNKNOWN";
 }
 
-int32_t gk_abi_version(void) { return 2; }
+int32_t gk_abi_version(void) { return 3; }
 
 gk_status gk_kv_append(const gk_shape* shape, const void* k_new, const void* v_new,
                        const float* cos, const float* sin, const float* k_scale,
@@ -200,8 +200,8 @@ static gk_status decode_attention(const gk_shape* shape, const void* q, const gk
                                   const float* k_scale, const float* v_scale,
                                   const float* cos, const float* sin, const int32_t* bt_full,
                                   const int32_t* bt_swa, const int32_t* pos, const int32_t* pos_w,
-                                  const uint8_t* active, void* out, float* out_f32,
-                                  void* workspace, size_t ws_bytes, void* stream,
+                                  const uint8_t* active, const float* sinks, void* out,
+                                  float* out_f32, void* workspace, size_t ws_bytes, void* stream,
                                   const AppendInputs* app) {
   gk_status st = check_shape(shape);
   if (st != GK_OK) return st;
@@ -245,6 +245,7 @@ static gk_status decode_attention(const gk_shape* shape, const void* q, const gk
   p.v_scale = v_scale;
   p.cosb = cos;
   p.sinb = sin;
+  p.sinks = sinks;
   p.bt_full = bt_full;
   p.bt_swa = bt_swa;
   p.hdr = reinterpret_cast<const int32_t*>(ws + L.hdr);
@@ -298,10 +299,10 @@ gk_status gk_decode_attn_stack(const gk_shape* shape, const void* q, const gk_kv
                                const float* k_scale, const float* v_scale,
                                const float* cos, const float* sin, const int32_t* bt_full,
                                const int32_t* bt_swa, const int32_t* pos, const int32_t* pos_w,
-                               const uint8_t* active, void* out, float* out_f32, void* workspace,
-                               size_t ws_bytes, void* stream) {
+                               const uint8_t* active, const float* sinks, void* out,
+                               float* out_f32, void* workspace, size_t ws_bytes, void* stream) {
   return decode_attention(shape, q, kv, k_scale, v_scale, cos, sin, bt_full, bt_swa, pos, pos_w,
-                          active, out, out_f32, workspace, ws_bytes, stream, nullptr);
+                          active, sinks, out, out_f32, workspace, ws_bytes, stream, nullptr);
 }
 
 gk_status gk_decode_step(const gk_shape* shape, const void* q, const void* k_new,
@@ -309,11 +310,11 @@ gk_status gk_decode_step(const gk_shape* shape, const void* q, const void* k_new
                          const float* k_scale, const float* v_scale, const int32_t* upd_full,
                          const int32_t* upd_swa, const int32_t* bt_full, const int32_t* bt_swa,
                          const int32_t* pos, const int32_t* pos_w, const uint8_t* active,
-                         const gk_kv_cache* kv, void* out, float* out_f32,
+                         const float* sinks, const gk_kv_cache* kv, void* out, float* out_f32,
                          void* workspace, size_t ws_bytes, void* stream) {
   const AppendInputs app = {k_new, v_new, upd_full, upd_swa};
   return decode_attention(shape, q, kv, k_scale, v_scale, cos, sin, bt_full, bt_swa, pos, pos_w,
-                          active, out, out_f32, workspace, ws_bytes, stream, &app);
+                          active, sinks, out, out_f32, workspace, ws_bytes, stream, &app);
 }
 
 gk_status gk_kv_budget(uint64_t total_bytes, uint64_t used_bytes, double gmu, double cap_fraction,

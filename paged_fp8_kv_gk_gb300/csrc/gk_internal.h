@@ -101,6 +101,7 @@ struct AttnParams {
   const float* v_scale;
   const float* cosb;
   const float* sinb;
+  const float* sinks;  // [NL, Hq] attention-sink logits or nullptr
   const int32_t* bt_full;
   const int32_t* bt_swa;
   const int32_t* hdr;

@@ -448,6 +448,18 @@ __device__ __forceinline__ void zero_row(const AttnParams& p, int layer, int b, 
   }
 }
 
+// Output scale of a head: v_scale / (l + 2^(sg - m)) with the head's
+// attention-sink logit sg (log2 units; none when `sink` is null), l the sum of
+// 2^(s - m) over its keys and m their reference maximum (log2 units).  When
+// sg > m numerator and denominator are scaled by 2^-(sg - m), so nothing
+// overflows.
+__device__ __forceinline__ float out_scale(float l, float m, const float* sink, float vscale) {
+  if (sink == nullptr) return vscale * __frcp_rn(l);
+  const float d = __ldg(sink) * 1.4426950408889634f - m;
+  const float e = ex2(-fabsf(d));
+  return d > 0.f ? vscale * e * __frcp_rn(fmaf(l, e, 1.f)) : vscale * __frcp_rn(l + e);
+}
+
 // Unit u covers plane u % planes of work entry e = u / planes.
 __device__ __forceinline__ void decode_unit(const AttnParams& p, int u, int4 e, UnitDesc& d) {
   const int pl = u - fdiv(u, p.fd_planes) * int(p.fd_planes.d);
@@ -1163,7 +1175,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       const int64_t out_row =
           ((int64_t(CU.layer) * p.Bt + CU.b) * p.Hq + CU.kvh * kGroup + 2 * qd) * kHeadDim + 8 * g;
       if (CU.ns == 1) {
-        const float i0 = vscale * __frcp_rn(l0), i1 = vscale * __frcp_rn(l1);
+        const float* snk =
+            p.sinks ? p.sinks + int64_t(CU.layer) * p.Hq + CU.kvh * kGroup + 2 * qd : nullptr;
+        const float i0 = out_scale(l0, mr0 * si0, snk, vscale);
+        const float i1 = out_scale(l1, mr1 * si1, snk ? snk + 1 : nullptr, vscale);
         float r0[8], r1[8];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
@@ -1248,7 +1263,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
               a1[c] = a1[c] * c1 + q1[c] * w1;
             }
           }
-          const float i0 = vscale * __frcp_rn(L0), i1 = vscale * __frcp_rn(L1);
+          const float* snk =
+              p.sinks ? p.sinks + int64_t(CU.layer) * p.Hq + CU.kvh * kGroup + 2 * qd : nullptr;
+          const float i0 = out_scale(L0, M0, snk, vscale);
+          const float i1 = out_scale(L1, M1, snk ? snk + 1 : nullptr, vscale);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             a0[c] *= i0;

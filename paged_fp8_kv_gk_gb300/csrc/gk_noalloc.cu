@@ -49,11 +49,11 @@ gk_status static_scratch_address(void** out) {
 extern "C" gk_status gk_decode_attn_stack_static(
     const gk_shape* shape, const void* q, const gk_kv_cache* kv, const float* k_scale, const float* v_scale, const float* cos, const float* sin,
     const int32_t* bt_full, const int32_t* bt_swa, const int32_t* pos, const int32_t* pos_w,
-    const uint8_t* active, void* out, float* out_f32, void* stream) {
+    const uint8_t* active, const float* sinks, void* out, float* out_f32, void* stream) {
   const size_t need = gk_attn_workspace_min_bytes(shape);
   if (need == 0)  // invalid or unsupported shape: the regular entry point says which
     return gk_decode_attn_stack(shape, q, kv, k_scale, v_scale, cos, sin, bt_full,
-                                bt_swa, pos, pos_w, active, out, out_f32, nullptr, 0, stream);
+                                bt_swa, pos, pos_w, active, sinks, out, out_f32, nullptr, 0, stream);
   if (need > GK_STATIC_SCRATCH_BYTES) return GK_ERR_WORKSPACE;
   void* scratch = nullptr;
   const gk_status st = static_scratch_address(&scratch);
@@ -62,6 +62,6 @@ extern "C" gk_status gk_decode_attn_stack_static(
   // at the start of every call, so the previous call's contents need no
   // clearing here.
   return gk_decode_attn_stack(shape, q, kv, k_scale, v_scale, cos, sin, bt_full,
-                              bt_swa, pos, pos_w, active, out, out_f32, scratch,
+                              bt_swa, pos, pos_w, active, sinks, out, out_f32, scratch,
                               GK_STATIC_SCRATCH_BYTES, stream);
 }

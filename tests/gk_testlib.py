@@ -58,7 +58,7 @@ class GpuStep:
     ``self.cache[j]`` is group j's [2, nb, kv, B, D] (K half, V half)."""
 
     def __init__(self, w: gi.Workload, c: gi.Control, step: dict, cache, device="cuda",
-                 k_layout: int = gk.GK_K_PACKED, form: str = "per_group"):
+                 k_layout: int = gk.GK_K_PACKED, form: str = "per_group", sinks=None):
         self.w, self.c = w, c
         dev = torch.device(device)
         self.shape = gk.Shape.make(**gi.shape_dict(w, c))
@@ -74,6 +74,7 @@ class GpuStep:
         self.upd_full = t(c.upd_full, torch.int32)
         self.upd_swa = t(c.upd_swa, torch.int32)
         self.active = t(c.active, torch.uint8)
+        self.sinks = None if sinks is None else t(sinks, torch.float32)
         self.q = step["q"].to(dev).contiguous()
         self.k_new = step["k_new"].to(dev).contiguous()
         self.v_new = step["v_new"].to(dev).contiguous()
@@ -109,17 +110,20 @@ class GpuStep:
                           self.k_scale, self.v_scale, self.upd_full, self.upd_swa, self.bt_full,
                           self.bt_swa, self.pos, self.pos_w, self.active, self.kv,
                           self.out, self.out_f32 if out_f32 else None,
-                          self.workspace if workspace is None else workspace, stream=stream)
+                          self.workspace if workspace is None else workspace, stream=stream,
+                          sinks=self.sinks)
 
     def attention(self, workspace=None, out_f32=True, stream=None):
         gk.gk_decode_attn_stack(self.shape, self.q, self.kv, self.k_scale, self.v_scale,
                                 self.cos, self.sin, self.bt_full, self.bt_swa, self.pos,
                                 self.pos_w, self.active, self.out,
                                 self.out_f32 if out_f32 else None,
-                                self.workspace if workspace is None else workspace, stream=stream)
+                                self.workspace if workspace is None else workspace, stream=stream,
+                                sinks=self.sinks)
 
 
-def oracle_step(w: gi.Workload, c: gi.Control, step: dict, cache, k_layout: int = 0):
+def oracle_step(w: gi.Workload, c: gi.Control, step: dict, cache, k_layout: int = 0,
+                sinks=None):
     """Oracle append + attention on host copies. Returns (out fp64, k_bufs, v_bufs).
     k_layout: 0 packed K view, 1 unpacked K."""
     sh = oracle.make_shape(**gi.shape_dict(w, c), k_layout=k_layout)
@@ -129,7 +133,8 @@ def oracle_step(w: gi.Workload, c: gi.Control, step: dict, cache, k_layout: int 
                           c.sin, c.k_scale, c.v_scale, c.upd_full, c.upd_swa, c.active, kb, vb)
     assert st == 0
     out, st = oracle.decode_attn_stack(sh, gi.bf16_bits(step["q"]), kb, vb, c.k_scale, c.v_scale,
-                                       c.cos, c.sin, c.bt_full, c.bt_swa, c.pos, c.pos_w, c.active)
+                                       c.cos, c.sin, c.bt_full, c.bt_swa, c.pos, c.pos_w, c.active,
+                                       sinks=sinks)
     assert st == 0
     return out, kb, vb
 
@@ -145,11 +150,11 @@ def gather_row_pool(w: gi.Workload, c: gi.Control, cache, j: int, b: int):
 
 
 def oracle_row_pair(w: gi.Workload, c: gi.Control, step_host: dict, pre_cache, j: int, b: int,
-                    kvhs=None, k_layout: int = 0):
+                    kvhs=None, k_layout: int = 0, sinks=None):
     """Oracle outputs for layers 2j and 2j+1 of row b from the generator's
     pre-append cache (see oracle.rows)."""
     kp, vp = gather_row_pool(w, c, pre_cache, j, b)
-    return oracle_rows.row_pair_from_pool(w, c, step_host, kp, vp, j, b, kvhs, k_layout)
+    return oracle_rows.row_pair_from_pool(w, c, step_host, kp, vp, j, b, kvhs, k_layout, sinks)
 
 
 def _k_codes(kbuf, nb, Hkv, B, D, pb, h, t, k_layout):

@@ -56,7 +56,7 @@ def _kv_struct(form="per_group", k_layout=gk.GK_K_PACKED, n=64, bad_index=None, 
 
 
 def test_version_and_status_strings():
-    assert gk.gk_abi_version() == 2
+    assert gk.gk_abi_version() == 3
     names = [gk.gk_status_str(i) for i in range(7)]
     assert names == ["GK_OK", "GK_ERR_INVALID_ARG", "GK_ERR_UNSUPPORTED", "GK_ERR_WORKSPACE",
                      "GK_ERR_CUDA", "GK_ERR_DEVICE_BOUNDS", "GK_ERR_BUDGET"]
@@ -129,25 +129,26 @@ def test_null_and_alignment_checks_before_launch():
     assert L.gk_kv_append(ctypes.byref(sh), *a) == gk.GK_ERR_INVALID_ARG
 
     # attention: nulls, then workspace checks (all before any launch)
-    att = [good, kv] + [good] * 10 + [None, good]   # q, kv, k_scale..out, out_f32, workspace
+    # q, kv, k_scale..active, sinks (optional), out, out_f32 (optional), workspace
+    att = [good, kv] + [good] * 9 + [None, good, None, good]
     ws_min = L.gk_attn_workspace_min_bytes(ctypes.byref(sh))
 
     def call(a, nbytes):
         return L.gk_decode_attn_stack(ctypes.byref(sh), *a, nbytes, None)
 
-    for i in range(12):
+    for i in list(range(11)) + [12]:
         a = list(att)
         a[i] = None
         assert call(a, ws_min) == gk.GK_ERR_INVALID_ARG, i
     a = list(att)
-    a[13] = None
+    a[14] = None
     assert call(a, ws_min) == gk.GK_ERR_WORKSPACE
     a = list(att)
-    a[13] = ctypes.c_void_p(0x10080)          # not 256-byte aligned
+    a[14] = ctypes.c_void_p(0x10080)          # not 256-byte aligned
     assert call(a, ws_min) == gk.GK_ERR_WORKSPACE
     assert call(att, ws_min - 256) == gk.GK_ERR_WORKSPACE
     a = list(att)
-    a[12] = ctypes.c_void_p(0x10004)          # misaligned out_f32
+    a[13] = ctypes.c_void_p(0x10004)          # misaligned out_f32
     assert call(a, ws_min) == gk.GK_ERR_INVALID_ARG
     assert L.gk_e4m3_quantize(None, ctypes.c_float(1.0), None, -1, None) == gk.GK_ERR_INVALID_ARG
 
@@ -177,8 +178,8 @@ def test_kv_form_exactly_one(case):
     assert L.gk_kv_append(ctypes.byref(sh), *([good] * 9), ctypes.byref(kvs), None) == \
         gk.GK_ERR_INVALID_ARG
     ws_min = L.gk_attn_workspace_min_bytes(ctypes.byref(sh))
-    assert L.gk_decode_attn_stack(ctypes.byref(sh), good, ctypes.byref(kvs), *([good] * 10), None,
-                                  good, ws_min, None) == gk.GK_ERR_INVALID_ARG
+    assert L.gk_decode_attn_stack(ctypes.byref(sh), good, ctypes.byref(kvs), *([good] * 9), None,
+                                  good, None, good, ws_min, None) == gk.GK_ERR_INVALID_ARG
 
 
 def test_binding_kv_forms_and_rank_inference():

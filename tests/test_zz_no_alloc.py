@@ -68,5 +68,5 @@ def test_static_scratch_rejects_shapes_beyond_its_size():
     kvs = gk.KvCacheC(k_bufs=ctypes.cast(arr, ctypes.c_void_p),
                       v_bufs=ctypes.cast(arr, ctypes.c_void_p), k_layout=gk.GK_K_PACKED)
     st = gk.lib().gk_decode_attn_stack_static(ctypes.byref(sh), good, ctypes.byref(kvs),
-                                              *([good] * 10), None, None)
+                                              *([good] * 9), None, good, None, None)
     assert st == gk.GK_ERR_WORKSPACE
