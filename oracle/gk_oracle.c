@@ -15,7 +15,7 @@
  *   [SDPA] scaled dot-product attention, softmax(q.k / sqrt(d)) . v, the plain
  *         definition; [RoPE] rotary position embedding in the rotate-half form.
  *
- * Readings taken where the pages are silent (all listed in the design doc as well):
+ * Readings taken where the pages are silent:
  *   R1  K packed layout: the trailing [.., block/2, d, 2] view interleaves tokens
  *       2p and 2p+1 of one channel, so K byte (pb, h, t, e) sits at
  *       ((pb*Hkv + h)*(B/2) + t/2)*(2D) + 2e + (t & 1).  V is never packed:
