@@ -141,8 +141,9 @@ typedef struct {
  *   V_{i/2}[(pb,h,t,e)] = E4M3(v_new[i,b,h,e] / v_scale[i])
  * E4M3 = round to nearest, ties to even mantissa, saturating to +-448; NaN -> 0x7F.
  * Inactive rows write nothing.  No other byte of any buffer changes.
- * Returns GK_ERR_INVALID_ARG for null pointers, inconsistent shapes or a kv
- * that does not hold exactly one form.
+ * Returns GK_ERR_INVALID_ARG for null pointers, inconsistent shapes, k_new,
+ * v_new, cos or sin not 16-byte aligned, or a kv that does not hold exactly
+ * one form.
  */
 gk_status gk_kv_append(const gk_shape *shape, const void *k_new, const void *v_new,
                        const float *cos, const float *sin, const float *k_scale,

@@ -149,7 +149,8 @@ gk_status gk_kv_append(const gk_shape* shape, const void* k_new, const void* v_n
   if (!k_new || !v_new || !cos || !sin || !k_scale || !v_scale || !upd_full || !upd_swa ||
       !active)
     return GK_ERR_INVALID_ARG;
-  if (!aligned16(k_new) || !aligned16(v_new)) return GK_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(cos) || !aligned16(sin))
+    return GK_ERR_INVALID_ARG;
   AppendParams p;
   memset(&p, 0, sizeof(p));
   st = resolve_kv(*shape, kv, p.kb, p.vb, &p.k_packed);
