@@ -123,6 +123,16 @@ REDUCED = {
     "block16_small": WORKLOADS["tiny"].replace(
         name="block16_small", num_layers=4, batch=5, num_q_heads=16, num_kv_heads=2,
         lengths="fixed:1,15,16,143,300", seed=17, num_blocks=None),
+    # the largest shapes the library accepts: batch 8192, 1024-token blocks,
+    # 128 layers (64 group buffers)
+    "max_batch": WORKLOADS["tiny"].replace(
+        name="max_batch", batch=8192, lengths="uniform:1,64", seed=27, num_blocks=None),
+    "max_block": WORKLOADS["tiny"].replace(
+        name="max_block", num_layers=4, batch=3, block_size=1024, lengths="fixed:1,1000,2500",
+        seed=28, num_blocks=None),
+    "max_layers": WORKLOADS["tiny"].replace(
+        name="max_layers", num_layers=128, batch=2, block_size=32, lengths="fixed:40,300",
+        seed=29, num_blocks=None, scale=None),
     # DI landing: prompt lengths on both sides of N % B == B - 1 (143, 159 with
     # N >= W; 127 below it), a one-token prompt and block-boundary lengths
     "di_small": WORKLOADS["gptoss_b64"].replace(

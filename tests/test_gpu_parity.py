@@ -19,7 +19,8 @@ import paged_fp8_kv_gk_gb300 as gk
 pytestmark = pytest.mark.gpu
 
 SMALL = ["tiny", "gptoss_small", "long_small", "ragged_small", "swa_small", "swa_small_sat",
-         "swa_small_peaky", "block16_small", "gk120b_rank_small", "block64_small"]
+         "swa_small_peaky", "block16_small", "gk120b_rank_small", "block64_small",
+         "max_batch", "max_block", "max_layers"]
 FULL = ["gptoss_b64", "long_ctx", "ragged_b256", "swa_b512"]
 
 
