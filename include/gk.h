@@ -181,8 +181,8 @@ size_t gk_attn_workspace_min_bytes(const gk_shape *shape);
  * it is overwritten by every call (do not share one workspace between calls
  * that may overlap on the device).
  * Returns GK_ERR_WORKSPACE for a missing/small/misaligned workspace,
- * GK_ERR_INVALID_ARG for null or non-16-byte-aligned tensors or a kv that does
- * not hold exactly one form.
+ * GK_ERR_INVALID_ARG for null or non-16-byte-aligned tensors (sinks: 4-byte)
+ * or a kv that does not hold exactly one form.
  */
 gk_status gk_decode_attn_stack(const gk_shape *shape, const void *q, const gk_kv_cache *kv,
                                const float *k_scale, const float *v_scale,

@@ -210,7 +210,7 @@ static gk_status decode_attention(const gk_shape* shape, const void* q, const gk
       !pos || !pos_w || !active || !out)
     return GK_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(out) || (out_f32 && !aligned16(out_f32)) || !aligned16(cos) ||
-      !aligned16(sin))
+      !aligned16(sin) || (reinterpret_cast<uintptr_t>(sinks) & 3u))
     return GK_ERR_INVALID_ARG;
   if (app && (!app->k_new || !app->v_new || !app->upd_full || !app->upd_swa ||
               !aligned16(app->k_new) || !aligned16(app->v_new)))

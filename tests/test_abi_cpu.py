@@ -150,6 +150,9 @@ def test_null_and_alignment_checks_before_launch():
     a = list(att)
     a[13] = ctypes.c_void_p(0x10004)          # misaligned out_f32
     assert call(a, ws_min) == gk.GK_ERR_INVALID_ARG
+    a = list(att)
+    a[11] = ctypes.c_void_p(0x10002)          # misaligned sinks
+    assert call(a, ws_min) == gk.GK_ERR_INVALID_ARG
     assert L.gk_e4m3_quantize(None, ctypes.c_float(1.0), None, -1, None) == gk.GK_ERR_INVALID_ARG
 
 
