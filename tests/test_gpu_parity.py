@@ -270,3 +270,22 @@ def test_full_size_parity(name):
             for (layer, kvh), ref in res.items():
                 sl = slice(kvh * G, (kvh + 1) * G)
                 tl.check_out(out[layer, b, sl], of[layer, b, sl], ref, f"{name} l{layer} b{b} h{kvh}")
+
+
+def test_full_size_repeat_bitwise():
+    """Split merges happen in split order whatever the arrival order: repeated
+    full-size calls give bit-identical outputs (and no device error)."""
+    w = gi.get("gptoss_b64")
+    c = gi.make_control(w)
+    st = gi.make_step(w, "cuda")
+    cache = gi.make_cache(w, c, "cuda")
+    g = tl.GpuStep(w, c, st, cache)
+    g.append()
+    g.attention()
+    torch.cuda.synchronize()
+    ref, refb = g.out_f32.clone(), g.out.clone()
+    for _ in range(20):
+        g.attention()
+        torch.cuda.synchronize()
+        assert torch.equal(g.out_f32, ref) and torch.equal(g.out, refb)
+    assert gk.gk_read_device_error() == 0
