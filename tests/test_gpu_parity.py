@@ -289,3 +289,33 @@ def test_full_size_repeat_bitwise():
         torch.cuda.synchronize()
         assert torch.equal(g.out_f32, ref) and torch.equal(g.out, refb)
     assert gk.gk_read_device_error() == 0
+
+
+@pytest.mark.parametrize("case", ["q_zero", "v_zero", "k_zero"])
+def test_degenerate_inputs(case):
+    """q = 0 (every score 0: the normaliser's all-zero branch; the output is
+    the mean of the values), V = 0 (output exactly 0), K = 0 (uniform weights)
+    -- against the oracle on the same inputs."""
+    w, c, st, cache = _make_cpu("gptoss_small")
+    st = {k: v.clone() for k, v in st.items()}
+    cache = [b.clone() for b in cache]
+    if case == "q_zero":
+        st["q"].zero_()
+    elif case == "v_zero":
+        st["v_new"].zero_()
+        for b in cache:
+            b[1].zero_()
+    else:
+        st["k_new"].zero_()
+        for b in cache:
+            b[0].zero_()
+    ref, _, _ = tl.oracle_step(w, c, st, cache)
+    g = tl.GpuStep(w, c, st, cache)
+    g.append()
+    g.attention()
+    torch.cuda.synchronize()
+    assert gk.gk_read_device_error() == 0
+    out, of = _f64(g.out), _f64(g.out_f32)
+    tl.check_out(out, of, ref, case)
+    if case == "v_zero":
+        assert (g.out_f32 == 0).all()
