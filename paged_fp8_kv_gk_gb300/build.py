@@ -51,11 +51,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not _stale():
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
+    # objects go to a directory of this process's own, so that concurrent
+    # builds (parallel test workers) never overwrite each other's files; the
+    # library itself is replaced atomically
+    objdir = os.path.join(BUILD_DIR, f"obj{os.getpid()}")
+    os.makedirs(objdir, exist_ok=True)
     nvcc = _nvcc()
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(objdir, src.replace(".cu", ".o"))
         log = obj + ".log"
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
         f = open(log, "w")
@@ -77,6 +82,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     subprocess.check_call([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"])
     os.replace(tmp, LIB_PATH)
+    for src in SOURCES:  # keep the ptxas reports (registers, spills) beside the library
+        log = os.path.join(objdir, src.replace(".cu", ".o.log"))
+        os.replace(log, os.path.join(BUILD_DIR, os.path.basename(log)))
+    shutil.rmtree(objdir, ignore_errors=True)
     return LIB_PATH
 
 

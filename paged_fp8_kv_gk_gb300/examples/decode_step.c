@@ -1,16 +1,19 @@
 /*
  * decode_step.c -- one decode step through the C ABI alone (include/gk.h), no
  * Python: the program reads a step's inputs from raw little-endian files in a
- * directory, uploads them, runs gk_kv_append and gk_decode_attn_stack on CUDA
- * device 0, checks the device error word and writes the output and the group
- * buffers back.
+ * directory, uploads them, runs gk_kv_append and gk_decode_attn_stack (or the
+ * single-launch gk_decode_step) on CUDA device 0, checks the device error word
+ * and writes the output and the group buffers back.
  *
- *   usage: decode_step <dir>
+ *   usage: decode_step <dir> [split|fused]
+ *     split (default): gk_kv_append, then gk_decode_attn_stack
+ *     fused:           gk_decode_step (append and attention in one launch)
  *   inputs  (in <dir>): shape.bin (gk_shape, 10 x int32), q.bin, k_new.bin,
  *     v_new.bin (bf16), cos.bin, sin.bin, k_scale.bin, v_scale.bin (fp32),
  *     bt_full.bin, bt_swa.bin, pos.bin, pos_w.bin, upd_full.bin, upd_swa.bin
  *     (int32), active.bin (uint8), cache_<j>.bin (group buffer j: K half then
- *     V half, uint8) for j < num_layers / 2
+ *     V half, uint8) for j < num_layers / 2; optional sinks.bin (fp32
+ *     [num_layers, num_q_heads] attention-sink logits)
  *   outputs (in <dir>): out.bin (bf16 [NL, Bt, Hq, D]), cache_out_<j>.bin
  *
  * Build (see the package's build step for libgk.so):
@@ -72,8 +75,11 @@ static void *upload(const char *dir, const char *name, size_t *size) {
 }
 
 int main(int argc, char **argv) {
-  if (argc != 2) {
-    fprintf(stderr, "usage: %s <dir>\n", argv[0]);
+  int fused = 0;
+  if (argc == 3 && strcmp(argv[2], "fused") == 0)
+    fused = 1;
+  else if (!(argc == 2 || (argc == 3 && strcmp(argv[2], "split") == 0))) {
+    fprintf(stderr, "usage: %s <dir> [split|fused]\n", argv[0]);
     return 1;
   }
   const char *dir = argv[1];
@@ -92,6 +98,22 @@ int main(int argc, char **argv) {
     if (!d[k]) {
       fprintf(stderr, "cannot read or upload %s\n", names[k]);
       return 1;
+    }
+  }
+  size_t sinks_bytes = 0;
+  const float *sinks = NULL;  /* optional */
+  {
+    char path[4096];
+    snprintf(path, sizeof(path), "%s/sinks.bin", dir);
+    FILE *f = fopen(path, "rb");
+    if (f) {
+      fclose(f);
+      sinks = (const float *)upload(dir, "sinks.bin", &sinks_bytes);
+      if (!sinks ||
+          sinks_bytes != (size_t)sh->num_layers * sh->num_q_heads * sizeof(float)) {
+        fprintf(stderr, "sinks.bin unreadable or of the wrong size\n");
+        return 1;
+      }
     }
   }
   const int groups = sh->num_layers / 2;
@@ -127,15 +149,24 @@ int main(int argc, char **argv) {
     return 2;
   }
 
-  gk_status st = gk_kv_append(sh, d[1], d[2], (const float *)d[3], (const float *)d[4],
-                              (const float *)d[5], (const float *)d[6], (const int32_t *)d[11],
-                              (const int32_t *)d[12], (const uint8_t *)d[13], &kv, NULL);
-  if (st == GK_OK)
-    st = gk_decode_attn_stack(sh, d[0], &kv, (const float *)d[5], (const float *)d[6],
-                              (const float *)d[3], (const float *)d[4], (const int32_t *)d[7],
-                              (const int32_t *)d[8], (const int32_t *)d[9],
-                              (const int32_t *)d[10], (const uint8_t *)d[13], NULL, out, NULL,
-                              ws, ws_bytes, NULL);
+  gk_status st;
+  if (fused) {
+    st = gk_decode_step(sh, d[0], d[1], d[2], (const float *)d[3], (const float *)d[4],
+                        (const float *)d[5], (const float *)d[6], (const int32_t *)d[11],
+                        (const int32_t *)d[12], (const int32_t *)d[7], (const int32_t *)d[8],
+                        (const int32_t *)d[9], (const int32_t *)d[10], (const uint8_t *)d[13],
+                        sinks, &kv, out, NULL, ws, ws_bytes, NULL);
+  } else {
+    st = gk_kv_append(sh, d[1], d[2], (const float *)d[3], (const float *)d[4],
+                      (const float *)d[5], (const float *)d[6], (const int32_t *)d[11],
+                      (const int32_t *)d[12], (const uint8_t *)d[13], &kv, NULL);
+    if (st == GK_OK)
+      st = gk_decode_attn_stack(sh, d[0], &kv, (const float *)d[5], (const float *)d[6],
+                                (const float *)d[3], (const float *)d[4], (const int32_t *)d[7],
+                                (const int32_t *)d[8], (const int32_t *)d[9],
+                                (const int32_t *)d[10], (const uint8_t *)d[13], sinks, out,
+                                NULL, ws, ws_bytes, NULL);
+  }
   uint32_t bits = 0;
   if (st == GK_OK) st = gk_read_device_error(NULL, &bits, 1);
   if (st != GK_OK) {
@@ -159,7 +190,7 @@ int main(int argc, char **argv) {
       return 2;
     }
   }
-  printf("decode_step ok: abi %d, %d layers x %d rows\n", gk_abi_version(), sh->num_layers,
-         sh->batch);
+  printf("decode_step ok (%s%s): abi %d, %d layers x %d rows\n", fused ? "fused" : "split",
+         sinks ? ", sinks" : "", gk_abi_version(), sh->num_layers, sh->batch);
   return 0;
 }

@@ -1,7 +1,9 @@
 """The C ABI used from C alone: paged_fp8_kv_gk_gb300/examples/decode_step.c
 (built here with the system C compiler against libgk.so and the CUDA runtime)
-runs one decode step from raw input files; its output and group buffers match
-the oracle (bf16 output within the parity tolerance, KV bytes bit-exact)."""
+runs one decode step from raw input files, as append + attention or as the
+single-launch step, with or without attention sinks; its output and group
+buffers match the oracle (bf16 output within the parity tolerance, KV bytes
+bit-exact)."""
 import os
 import shutil
 import subprocess
@@ -40,13 +42,13 @@ def _write(d, name, a):
     np.ascontiguousarray(a).tofile(os.path.join(d, name))
 
 
-@pytest.mark.parametrize("name", ["tiny", "gptoss_small", "block16_small"])
-def test_c_program_step_matches_oracle(exe, tmp_path, name):
+def write_step_dir(d, name, with_sinks=False):
+    """Write one step's inputs for the C program into directory d; returns
+    (workload, control, step, cache, sinks or None)."""
     w = gi.get(name)
     c = gi.make_control(w)
     st = gi.make_step(w, "cpu")
     cache = gi.make_cache(w, c, "cpu")
-    d = str(tmp_path)
     sh = gk.Shape.make(**gi.shape_dict(w, c))
     with open(os.path.join(d, "shape.bin"), "wb") as f:
         f.write(bytes(sh))
@@ -59,15 +61,29 @@ def test_c_program_step_matches_oracle(exe, tmp_path, name):
     _write(d, "active.bin", np.asarray(c.active, np.uint8))
     for j, b in enumerate(cache):
         _write(d, f"cache_{j}.bin", b.numpy())
+    sinks = gi.make_sinks(w) if with_sinks else None
+    if sinks is not None:
+        _write(d, "sinks.bin", sinks)
+    return w, c, st, cache, sinks
+
+
+@pytest.mark.parametrize("name,mode,with_sinks", [
+    ("tiny", "split", False), ("gptoss_small", "split", False), ("block16_small", "split", False),
+    ("gptoss_small", "fused", False), ("ragged_small", "fused", True),
+    ("block16_small", "split", True)])
+def test_c_program_step_matches_oracle(exe, tmp_path, name, mode, with_sinks):
+    d = str(tmp_path)
+    w, c, st, cache, sinks = write_step_dir(d, name, with_sinks)
     env = dict(os.environ)
     env["LD_LIBRARY_PATH"] = ":".join([gkbuild.BUILD_DIR, os.path.join(CUDA, "lib64"),
                                        env.get("LD_LIBRARY_PATH", "")])
-    r = subprocess.run([exe, d], env=env, capture_output=True, text=True, timeout=300)
+    r = subprocess.run([exe, d, mode], env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
-    ref, kb_ref, vb_ref = tl.oracle_step(w, c, st, cache)
+    assert mode in r.stdout
+    ref, kb_ref, vb_ref = tl.oracle_step(w, c, st, cache, sinks=sinks)
     out_bits = np.fromfile(os.path.join(d, "out.bin"), np.uint16).reshape(ref.shape)
     out = (out_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    tl.check_out(out, None, ref, f"C program {name}")
+    tl.check_out(out, None, ref, f"C program {name} {mode}")
     for j in range(len(cache)):
         got = np.fromfile(os.path.join(d, f"cache_out_{j}.bin"), np.uint8)
         half = got.size // 2

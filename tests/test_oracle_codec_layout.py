@@ -83,6 +83,29 @@ def test_encode_exhaustive_relevant_range():
             assert bad.size == 0, (e, s, x[bad[:5]], got[bad[:5]], exp[bad[:5]])
 
 
+def test_encode_outside_that_range_is_zero_or_saturated():
+    """The rest of the fp32 bit patterns, by closed form (OCP E4M3 fn, RNE,
+    satfinite): |x| < 2^-12 lies below half the smallest subnormal (2^-10)
+    and encodes to a zero of the same sign; |x| >= 2^10 (infinities included)
+    lies past 448 and encodes to +-448 (0x7E / 0xFE); NaNs encode to 0x7F.
+    Every exponent field is visited with a strided sample of its mantissas
+    plus both ends."""
+    mant = np.unique(np.concatenate([np.arange(0, 1 << 23, 4099, dtype=np.uint32),
+                                     np.array([0, 1, (1 << 23) - 1], np.uint32)]))
+    for e in list(range(0, 127 - 12)) + list(range(127 + 10, 256)):
+        for s in (0, 1):
+            bits = (np.uint32(s) << np.uint32(31)) | (np.uint32(e) << np.uint32(23)) | mant
+            x = bits.view(np.float32)
+            got = oracle.e4m3_encode(x)
+            if e == 255:
+                want = np.where(mant == 0, np.uint8(0x7E | (s << 7)), np.uint8(0x7F))
+            elif e >= 127 + 10:
+                want = np.full(mant.size, 0x7E | (s << 7), np.uint8)
+            else:
+                want = np.full(mant.size, s << 7, np.uint8)
+            assert np.array_equal(got, want), (e, s)
+
+
 def test_encode_random_bit_patterns_and_specials():
     rng = np.random.default_rng(123)
     bits = rng.integers(0, 1 << 32, size=1 << 22, dtype=np.uint64).astype(np.uint32)
