@@ -93,6 +93,69 @@ def test_oracle_step_matches_independent_restatement(name):
     assert np.max(np.abs(out - ref)) < 1e-11
 
 
+@pytest.mark.parametrize("name", ["gptoss_small", "ragged_small", "block16_small"])
+def test_each_row_equals_that_row_alone(name):
+    """Rows of a batch are independent problems: the whole-step result for
+    row b equals (bit for bit) the step run on a batch holding row b alone
+    (its q, cos/sin, table rows, positions and activity, the same caches)."""
+    w, c, st, cache = _setup(name)
+    q = gi.bf16_bits(st["q"])
+    kb, vb = _np_bufs(cache)
+    args = lambda rows: (q[:, rows], kb, vb, c.k_scale, c.v_scale, c.cos[rows], c.sin[rows],  # noqa: E731
+                         c.bt_full[rows], c.bt_swa[rows], c.pos[rows], c.pos_w[rows], c.active[rows])
+    full, status = oracle.decode_attn_stack(_shape(w, c), *args(slice(None)))
+    assert status == 0
+    d = gi.shape_dict(w, c)
+    d["batch"] = 1
+    sh1 = oracle.make_shape(**d)
+    for b in range(w.batch):
+        one, status = oracle.decode_attn_stack(sh1, *args(slice(b, b + 1)))
+        assert status == 0
+        assert np.array_equal(one[:, 0], full[:, b]), (name, b)
+
+
+@pytest.mark.parametrize("name", ["gptoss_small", "max_layers"])
+def test_layer_reads_group_buffer_i_over_2(name):
+    """Layer i reads group buffer i // 2 with its own V scale ("Kernel
+    contract"): fill every V byte of group buffer j with the code of 2^(j % 4)
+    and the output of every active (layer, row, head) is exactly
+    2^((i // 2) % 4) * v_scale[i], whatever the keys (constant values)."""
+    w, c, st, cache = _setup(name)
+    q = gi.bf16_bits(st["q"])
+    kb, vb = _np_bufs(cache)
+    vb = [np.full_like(v, 0x38 + 8 * (j % 4)) for j, v in enumerate(vb)]   # 1, 2, 4, 8
+    out, status = oracle.decode_attn_stack(_shape(w, c), q, kb, vb, c.k_scale, c.v_scale, c.cos,
+                                           c.sin, c.bt_full, c.bt_swa, c.pos, c.pos_w, c.active)
+    assert status == 0
+    for i in range(w.num_layers):
+        want = 2.0 ** ((i // 2) % 4) * float(c.v_scale[i])
+        assert (out[i, c.active == 1] == want).all(), (name, i)
+
+
+@pytest.mark.parametrize("name", ["gptoss_small", "block16_small"])
+def test_step_is_per_unit_attention_on_group_buffer_i_over_2(name):
+    """The whole-step routine is the per-(layer, row, kv head) attention (whose
+    arithmetic the closed-form and contiguous-cache pins fix) applied with
+    group buffer i // 2 ("Kernel contract"), its output placed at heads
+    kvh*G .. kvh*G + G - 1 of row b, layer i."""
+    w, c, st, cache = _setup(name)
+    q = gi.bf16_bits(st["q"])
+    kb, vb = _np_bufs(cache)
+    sh = _shape(w, c)
+    out, status = oracle.decode_attn_stack(sh, q, kb, vb, c.k_scale, c.v_scale, c.cos, c.sin,
+                                           c.bt_full, c.bt_swa, c.pos, c.pos_w, c.active)
+    assert status == 0
+    G = w.num_q_heads // w.num_kv_heads
+    for i in range(w.num_layers):
+        for b in range(w.batch):
+            for kvh in range(w.num_kv_heads):
+                one, status = oracle.attn_one(sh, q, kb[i // 2], vb[i // 2], c.k_scale, c.v_scale,
+                                              c.cos, c.sin, c.bt_full, c.bt_swa, c.pos, c.pos_w,
+                                              c.active, i, b, kvh)
+                assert status == 0
+                assert np.array_equal(out[i, b, kvh * G:(kvh + 1) * G], one), (i, b, kvh)
+
+
 def test_inactive_rows_are_zero():
     w, c, st, cache = _setup("ragged_small")
     assert (c.active == 0).any()
@@ -177,16 +240,18 @@ def test_window_layer_equals_last_W_keys_of_contiguous_cache(L):
     """P6: layer 0 through the trimmed table and window-frame position equals
     attention over the last W positions of the contiguous cache; layer 1
     through the full table equals attention over all L positions.  Lengths
-    cover L % B == B - 1 and the window start at several block offsets."""
+    cover L % B == B - 1 and the window start at several block offsets.  K and
+    V carry different scales."""
     B, W, G, D = 16, 128, 4, 64
     sh, q, kbuf, vbuf, sc, cos, sin, ctl, kc, vc = _window_case(L, B=B, W=W, G=G, seed=L)
+    sv = np.array([1 / 4, 1 / 128], np.float32)
     for layer, keys in ((0, np.arange(max(0, L - W), L)), (1, np.arange(L))):
         for kvh in range(2):
-            out, st = oracle.attn_one(sh, q, kbuf, vbuf, sc, sc, cos, sin, ctl["bt_full"],
+            out, st = oracle.attn_one(sh, q, kbuf, vbuf, sc, sv, cos, sin, ctl["bt_full"],
                                       ctl["bt_swa"], ctl["pos"], ctl["pos_w"], ctl["active"],
                                       layer, 0, kvh)
             assert st == 0
-            ref = _contig_attention(q[layer, 0], kc, vc, sc[layer], sc[layer], cos, sin, keys, kvh, G, D)
+            ref = _contig_attention(q[layer, 0], kc, vc, sc[layer], sv[layer], cos, sin, keys, kvh, G, D)
             assert np.max(np.abs(out - ref)) < 1e-11, (L, layer, kvh)
 
 
@@ -318,8 +383,12 @@ def test_append_touches_exactly_the_update_slots(name):
 def test_append_codes_match_library_cast_and_values():
     """Read back through the page's packed view: V codes equal torch's float8
     cast of v / scale; decoded K values are within half an E4M3 step of the
-    exact rotation of k / scale, and values past 448 saturate."""
+    exact rotation of k / scale, and values past 448 saturate.  The V scales
+    are set apart from the K scales (the workload uses one scale for both),
+    so that each half is checked against its own scale."""
     w, c, st, cache = _setup("swa_small_sat")
+    c.v_scale = np.array([2.0 ** -(2 + i % 4) for i in range(w.num_layers)], np.float32)
+    assert not np.array_equal(c.v_scale, c.k_scale)
     kb, vb, _ = _append(w, c, st, cache)
     B, Hkv, D = w.block_size, w.num_kv_heads, w.head_dim
     kf = st["k_new"].to(torch.float64).numpy()
