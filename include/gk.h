@@ -31,6 +31,18 @@
  *     launches are chained by programmatic dependent launch, which capture
  *     keeps).  The first call on a device sets kernel attributes and caches
  *     device properties: make it before any capture.
+ *   - Programmatic dependent launch at the start of an attention call: its
+ *     first kernel (the planner) is launched as a programmatic dependent of
+ *     whatever kernel precedes it in the stream and reads `active`, `pos` and
+ *     `pos_w` as soon as it runs; everything else (q, the cache, the tables,
+ *     the scales) is read only after that preceding kernel has completed.  A
+ *     preceding kernel can let the planner start early only by opening
+ *     dependent launch itself (griddepcontrol.launch_dependents, or
+ *     cudaTriggerProgrammaticLaunchCompletion); kernels that never do so,
+ *     which is the common case, are always complete first.  So a kernel that
+ *     writes a call's `active`, `pos` or `pos_w` must not open dependent
+ *     launch before those writes.  (gk_kv_append opens it early and writes
+ *     none of them.)
  *   - Errors: every entry point returns a gk_status and never aborts, traps or
  *     prints.  Argument checks run on the host before anything is enqueued; a
  *     failed check enqueues nothing.  Launch failures map to GK_ERR_CUDA.
