@@ -154,6 +154,12 @@ PROFILE = {
     "gptoss_b8": WORKLOADS["gptoss_b64"].replace(name="gptoss_b8", batch=8, seed=22),
     "gptoss_b16": WORKLOADS["gptoss_b64"].replace(name="gptoss_b16", batch=16, seed=23),
     "swa_b128": WORKLOADS["swa_b512"].replace(name="swa_b128", batch=128, seed=24),
+    # latency end of the 36-layer shapes: one or eight rows of 8192 tokens
+    # (0.15 / 1.2 GB of KV), where the fixed costs of a call weigh most
+    "gptoss_b1_8k": WORKLOADS["gptoss_b64"].replace(name="gptoss_b1_8k", batch=1,
+                                                     lengths="all:8192", seed=30),
+    "gptoss_b8_8k": WORKLOADS["gptoss_b64"].replace(name="gptoss_b8_8k", batch=8,
+                                                     lengths="all:8192", seed=31),
 }
 
 
