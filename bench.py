@@ -461,6 +461,26 @@ def run_gk(args):
     if gk.gk_read_device_error() != 0:
         raise RuntimeError("device error word set during warm-up")
 
+    # L2: a step whose KV is not well above the L2 size would find part of it
+    # still cached from the step before; such steps are timed one by one with
+    # a write of twice the L2 size between them, outside the timed events
+    kv_bytes = gi.kv_bytes_read(w, c)
+    l2_bytes = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    flush = args.flush_l2 == "on" or (args.flush_l2 == "auto" and kv_bytes < 2 * l2_bytes)
+    flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush else None
+    if flush:
+        l2_note = (f"L2 flushed before every timed step ({2 * l2_bytes / 1e6:.0f} MB write, outside "
+                   f"the events; {kv_bytes / 1e9:.3f} GB KV read per step; e2e unflushed)")
+    elif kv_bytes >= 2 * l2_bytes:
+        l2_note = f"inputs larger than L2: {kv_bytes / 1e9:.2f} GB KV read per step"
+    else:
+        l2_note = (f"L2 not flushed (--flush-l2 off): {kv_bytes / 1e9:.3f} GB KV read per step, "
+                   f"under twice the L2 size")
+
+    def l2_flush(k):
+        if flush:
+            flush_buf.fill_(k & 0xff)
+
     # ---- timed loop 1: whole steps (append + attention), events only at the
     # two ends so that nothing sits between the kernels of a step
     ev0 = torch.cuda.Event(enable_timing=True)
@@ -471,22 +491,35 @@ def run_gk(args):
     torch.cuda.synchronize(dev)
     clocks.start()
     clocks.mark_begin()
-    ev0.record(stream)
-    for k in range(K):
-        one_step()
-    ev1.record(stream)
+    if flush:
+        s0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        s1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        for k in range(K):
+            l2_flush(k)
+            s0[k].record(stream)
+            one_step()
+            s1[k].record(stream)
+    else:
+        ev0.record(stream)
+        for k in range(K):
+            one_step()
+        ev1.record(stream)
     torch.cuda.synchronize(dev)
     clocks.mark_end()
     clk = clocks.stop()
     if dist:
         dist.barrier()
-    elapsed_ms = ev0.elapsed_time(ev1)
+    if flush:
+        elapsed_ms = sum(s0[k].elapsed_time(s1[k]) for k in range(K))
+    else:
+        elapsed_ms = ev0.elapsed_time(ev1)
 
     # ---- timed loop 2: the attention call (planner + persistent kernel) alone,
     # an event pair around every launch, for the roofline of the dominant kernel
     a0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     a1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     for k in range(K):
+        l2_flush(k)
         a0[k].record(stream)
         attention()
         a1[k].record(stream)
@@ -496,6 +529,7 @@ def run_gk(args):
     attn_med = statistics.median(attn_all)
     # the append alone, for the record
     for k in range(K):
+        l2_flush(k)
         a0[k].record(stream)
         append()
         a1[k].record(stream)
@@ -516,7 +550,6 @@ def run_gk(args):
         raise RuntimeError("device error word set during the timed region")
 
     # ---- roofline of the attention call
-    kv_bytes = gi.kv_bytes_read(w, c)
     qo = gi.qo_bytes(w, c)
     alg_bytes = kv_bytes + qo
     peak, peak_kind = measured_peaks()
@@ -529,8 +562,7 @@ def run_gk(args):
         "precision": "KV E4M3 codes; q/out bf16; QK^T and PV on f16 tensor-core MMA with fp32 "
                      "accumulation; fp32 online softmax",
         "data": "synthetic (seeded gk_inputs workload)",
-        "config": workload_config(w, c, f"inputs larger than L2: {kv_bytes / 1e9:.2f} GB KV read per step",
-                                  kv_layout_desc(args.k_layout, args.kv_form)),
+        "config": workload_config(w, c, l2_note, kv_layout_desc(args.k_layout, args.kv_form)),
         "impl": "gk",
         "attn_ms": round(attn_ms, 4),
         "attn_ms_median": round(attn_med, 4),
@@ -708,6 +740,9 @@ def main(argv=None):
     ap.add_argument("--record-traffic", metavar="LAUNCHES_CSV", default=None,
                     help="store the attention kernel's DRAM bytes per launch from an ncu launch "
                          "list of --workload into profiles/attn_traffic.json, then exit")
+    ap.add_argument("--flush-l2", choices=["auto", "on", "off"], default="auto",
+                    help="write twice the L2 size before every timed step (auto: when the KV "
+                         "read per step is under twice the L2 size)")
     ap.add_argument("--ws-min", action="store_true",
                     help="use the minimum attention workspace (no split-KV chunks)")
     args = ap.parse_args(argv)
