@@ -49,6 +49,7 @@ enum HdrWord {
   kHdrSplit = 4,        // split length in tokens
   kHdrNEntries = 5,
   kHdrTotalSplits = 6,
+  kHdrPieces = 7,       // pieces cut from chunks of long rows for the last wave (0: none)
   kHdrWords = 64
 };
 

@@ -166,6 +166,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   int32_t* Ls = plan_sm;          // clamped context length per row (0 = no work)
   int32_t* Pw = plan_sm + p.Bt;   // window-frame position per row
   __shared__ long long s_units[kSplitCands], s_need[kSplitCands];
+  __shared__ long long s_full[kSplitCands], s_remtok[kSplitCands];
+  __shared__ int s_ne[kSplitCands], s_maxnf[kSplitCands];
+  __shared__ int s_conv[3];  // chunks cut per eligible row, rows cutting one more, pieces
+  __shared__ int s_erank[kPlanWarps];
   __shared__ long long s_red[3][kPlanWarps];
   __shared__ int s_bucket[kRemBuckets];
   __shared__ int4 s_scan[kPlanWarps];
@@ -220,20 +224,35 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   for (int k = wid; k < kSplitCands; k += kPlanWarps) {
     const int sh = 9 + k;  // log2 of kMinSplit << k
     const long long S = 1ll << sh;
-    long long units = 0, need = 0;
+    long long units = 0, need = 0, full = 0, remtok = 0;
+    int ne = 0, maxnf = 0;
     for (int b = lane; b < p.Bt; b += 32) {
       const int L = Ls[b];
       if (L > 0) {
         const long long c = (L + S - 1) >> sh;
+        const int nf = int(L >> sh);
         units += c;
         if (L > S) need += c;
+        full += nf;
+        remtok += L & (S - 1);
+        ne += nf >= 2;
+        maxnf = max(maxnf, nf);
       }
     }
     units = warp_sum64(units);
     need = warp_sum64(need);
+    full = warp_sum64(full);
+    remtok = warp_sum64(remtok);
+    ne = warp_sum(ne);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) maxnf = max(maxnf, __shfl_xor_sync(kFull, maxnf, o));
     if (lane == 0) {
       s_units[k] = units;
       s_need[k] = need;
+      s_full[k] = full;
+      s_remtok[k] = remtok;
+      s_ne[k] = ne;
+      s_maxnf[k] = maxnf;
     }
   }
   __syncthreads();
@@ -252,8 +271,59 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     while (k < kSplitCands - 1 && ((long long)kMinSplit << k) * kMaxSplitsPerRow < Lmax) ++k;
     while (k < kSplitCands - 1 && s_need[k] > p.cap) ++k;
     s_S_log = k;
+    // Last wave.  Equal chunks give full * planes units of one size; when
+    // that is not a whole number of waves over the warps and the smaller
+    // units (remainders, window units) cannot fill the idle part of the last
+    // wave, cut the last chunks of the rows with two or more of them into
+    // p pieces (largest-first order runs them at the end), keeping whole
+    // waves of full chunks.  Rows stay within kMaxSplitsPerRow chunks and
+    // the partial records within the workspace.
+    int conv_c = 0, conv_x = 0, conv_p = 0;
+    const long long Sk = (long long)kMinSplit << k;
+    const long long cunits = s_full[k] * planes;
+    const long long q = cunits / warps, rem = cunits - q * warps;
+    const long long gap = (warps - rem) * Sk;                    // idle token slots
+    const long long small = (s_remtok[k] + NAct * p.W) * planes;  // work in smaller units
+    if (rem > 0 && small < gap && s_ne[k] > 0) {
+      // cv chunks in all, spread over the eligible rows in row order (fewer
+      // if a row would pass kMaxSplitsPerRow chunks or the records the
+      // workspace holds)
+      const long long cv = s_full[k] - (q * warps) / planes;
+      for (int pp = int(min(8ll, Sk / kMinSplit)); pp >= 2; pp >>= 1) {
+        const long long per_row = (kMaxSplitsPerRow - 1 - s_maxnf[k]) / (pp - 1);
+        const long long room = (p.cap - s_need[k]) / (pp - 1);
+        const long long cvp = min(cv, min(per_row * s_ne[k], room));
+        if (cvp >= 1) {
+          conv_c = int(cvp / s_ne[k]);
+          conv_x = int(cvp - conv_c * s_ne[k]);
+          conv_p = pp;
+          break;
+        }
+      }
+    }
+    s_conv[0] = conv_c;
+    s_conv[1] = conv_x;
+    s_conv[2] = conv_p;
   }
   __syncthreads();
+  const int conv_c = s_conv[0], conv_x = s_conv[1], conv_p = s_conv[2];
+  // rank of this thread's first row among the rows with two or more full
+  // chunks (the first conv_x of them cut one chunk more)
+  int erank = 0;
+  if (conv_p > 0) {
+    int e = 0;
+    for (int b = b_lo; b < b_hi; ++b) e += (Ls[b] >> (9 + s_S_log)) >= 2;
+    int inc = e;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += y;
+    }
+    if (lane == 31) s_erank[wid] = inc;
+    __syncthreads();
+    erank = inc - e;
+    for (int w = 0; w < wid; ++w) erank += s_erank[w];
+  }
   const int S_log = s_S_log;
   const int S_sh = 9 + S_log;  // S = 2^S_sh
   const long long S = 1ll << S_sh;
@@ -262,17 +332,33 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
 
   // per-thread counts -> one packed exclusive scan: (full chunks, split
   // records, active rows, remainders)
+  // a row's chunks: nf - cut full chunks, then cut * conv_p pieces, then the
+  // remainder; split indices follow the keys
+  const int piece_len = conv_p > 0 ? int(S) / conv_p : 0;
+  const int piece_bucket = conv_p > 0 ? kRemBuckets - 1 - (piece_len >> bshift) : 0;
+  auto cut_of = [&](int nf, int& rank) {
+    if (conv_p == 0 || nf < 2) return 0;
+    const int c = conv_c + (rank < conv_x ? 1 : 0);
+    ++rank;
+    return min(c, nf);
+  };
   int4 cnt = make_int4(0, 0, 0, 0);
+  int rk = erank;
   for (int b = b_lo; b < b_hi; ++b) {
     const int L = Ls[b];
     if (L > 0) {
-      const int nf = int(L >> S_sh), r = int(L & (S - 1)), ns = nf + (r > 0);
-      cnt.x += nf;
+      const int nf = int(L >> S_sh), r = int(L & (S - 1)), cut = cut_of(nf, rk);
+      const int ns = nf + cut * (conv_p - 1) + (r > 0);
+      cnt.x += nf - cut;
       cnt.y += ns > 1 ? ns : 0;
       cnt.z += 1;
       if (r > 0) {
         cnt.w += 1;
         atomicAdd(&s_bucket[kRemBuckets - 1 - (r >> bshift)], 1);  // largest first
+      }
+      if (cut > 0) {
+        cnt.w += cut * conv_p;
+        atomicAdd(&s_bucket[piece_bucket], cut * conv_p);
       }
     }
   }
@@ -334,15 +420,26 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   int ip = b_lo - ap;     // inactive rows before this thread's rows
   (void)R;
 
+  rk = erank;
   for (int b = b_lo; b < b_hi; ++b) {
     const int L = Ls[b];
     if (L > 0) {
-      const int nf = int(L >> S_sh), r = int(L & (S - 1)), ns = nf + (r > 0);
-      for (int s = 0; s < nf; ++s)
+      const int nf = int(L >> S_sh), r = int(L & (S - 1)), cut = cut_of(nf, rk);
+      const int ns = nf + cut * (conv_p - 1) + (r > 0);
+      const int nk = nf - cut;  // full chunks kept
+      for (int s = 0; s < nk; ++s)
         p.edesc[fp++] = make_int4(b, int(s * S), int((s + 1) * S), s | (ns << 16));
+      if (cut > 0) {
+        const int np = cut * conv_p;
+        const int slot = atomicAdd(&s_bucket[piece_bucket], np);
+        for (int i = 0; i < np; ++i) {
+          const int t0 = int(nk * S) + i * piece_len;
+          p.edesc[A + slot + i] = make_int4(b, t0, t0 + piece_len, (nk + i) | (ns << 16));
+        }
+      }
       if (r > 0) {
         const int slot = atomicAdd(&s_bucket[kRemBuckets - 1 - (r >> bshift)], 1);
-        p.edesc[A + slot] = make_int4(b, int(nf * S), L, nf | (ns << 16));
+        p.edesc[A + slot] = make_int4(b, int(nf * S), L, (ns - 1) | (ns << 16));
       }
       if (ns > 1) {
         p.part_base[b] = sp;
@@ -372,6 +469,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     p.hdr[kHdrSplit] = int(S);
     p.hdr[kHdrNEntries] = NEF + NA;
     p.hdr[kHdrTotalSplits] = TS;
+    p.hdr[kHdrPieces] = conv_p > 0 ? (conv_c * s_ne[s_S_log] + conv_x) * conv_p : 0;
   }
   // This grid may have started while the kernel before it (the KV append)
   // was still running; it completes only after that kernel has, so the

@@ -60,7 +60,7 @@ def test_fused_equals_two_calls_bitwise():
     assert torch.equal(a.out, b.out) and torch.equal(a.out_f32, b.out_f32)
 
 
-@pytest.mark.parametrize("name", ["gptoss_b64", "swa_b512"])
+@pytest.mark.parametrize("name", ["gptoss_b64", "swa_b512", "long_ctx"])
 def test_fused_step_full_size(name):
     w = gi.get(name)
     c = gi.make_control(w)

@@ -103,6 +103,31 @@ def test_split_and_unsplit_agree(name):
     assert gk.gk_read_device_error() == 0
 
 
+@pytest.mark.parametrize("name,step", [("long_cut_small", "split"), ("long_cut_small", "fused")])
+def test_last_wave_pieces(name, step):
+    """Two long rows: equal chunks would leave a partial last wave, so the
+    planner cuts chunks of those rows into pieces that run at the end (header
+    word 7 counts them).  Pieces change only where the splits fall: KV bytes
+    stay bit-exact and the output meets the tolerance, in the two-launch and
+    the single-launch step (whose last piece of each row appends the token)."""
+    w, c, st, cache = _make_cpu(name)
+    ref, kb_ref, vb_ref = tl.oracle_step(w, c, st, cache)
+    g = tl.GpuStep(w, c, st, cache)
+    if step == "fused":
+        g.step()
+    else:
+        g.append()
+        g.attention()
+    torch.cuda.synchronize()
+    assert gk.gk_read_device_error() == 0
+    hdr = g.workspace[:256].view(torch.int32).cpu().numpy()
+    assert hdr[7] > 0 and hdr[6] > 0, hdr[:8]
+    for j in range(len(g.cache)):
+        assert np.array_equal(g.cache[j][0].cpu().numpy().reshape(-1), kb_ref[j]), ("K", j)
+        assert np.array_equal(g.cache[j][1].cpu().numpy().reshape(-1), vb_ref[j]), ("V", j)
+    tl.check_out(_f64(g.out), _f64(g.out_f32), ref, f"{name}/{step}")
+
+
 def test_repeat_is_bitwise_deterministic():
     w, c, st, cache = _make_cpu("long_small")
     g = tl.GpuStep(w, c, st, cache)
