@@ -101,10 +101,11 @@ REDUCED = {
         name="gptoss_small", num_layers=4, batch=6, lengths="fixed:1,31,32,159,160,1100", seed=12),
     "long_small": WORKLOADS["long_ctx"].replace(
         name="long_small", num_layers=2, batch=2, lengths="all:9000", seed=13),
-    # two rows long enough that equal chunks leave a partial last wave, so the
-    # planner cuts chunks of the long rows into pieces for it
+    # three rows long enough that equal chunks leave a partial last wave, so
+    # the planner cuts chunks of the long rows into pieces for it (checked on
+    # sampled rows: the whole-step oracle would take about a minute)
     "long_cut_small": WORKLOADS["long_ctx"].replace(
-        name="long_cut_small", num_layers=4, batch=2, lengths="all:40000", seed=32),
+        name="long_cut_small", num_layers=16, batch=3, lengths="all:36000", seed=32),
     "ragged_small": WORKLOADS["ragged_b256"].replace(
         name="ragged_small", num_layers=4, batch=12, lengths="loguniform:1,3000", seed=14,
         inactive_frac=0.25),

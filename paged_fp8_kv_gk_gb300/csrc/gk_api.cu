@@ -77,6 +77,8 @@ static gk_status resolve_kv(const gk_shape& s, const gk_kv_cache* kv, uint8_t** 
   return GK_OK;
 }
 
+static int64_t cmax_of(const gk_shape& s) { return int64_t(s.batch) * kMaxSplitsPerRow; }
+
 WsLayout ws_layout(const gk_shape& s, size_t ws_bytes) {
   WsLayout L;
   const int64_t planes = int64_t(s.num_layers / 2) * s.num_kv_heads;
@@ -109,11 +111,11 @@ WsLayout ws_layout(const gk_shape& s, size_t ws_bytes) {
   place(0);
   const size_t fixed = L.total;
   int64_t cap = 0;
-  if (ws_bytes > fixed + 512) {
+  if (ws_bytes > fixed + 512)
     cap = int64_t((ws_bytes - fixed - 512) / (size_t(planes) * rec + sizeof(int4)));
-    const int64_t cmax = int64_t(s.batch) * kMaxSplitsPerRow;
-    if (cap > cmax) cap = cmax;
-  }
+  // the estimate above can fall one record short (alignment slack): start
+  // two above it and step down to the largest capacity that fits
+  cap = cap + 2 < cmax_of(s) ? cap + 2 : cmax_of(s);
   place(cap);
   while (cap > 0 && L.total > ws_bytes) place(--cap);
   return L;

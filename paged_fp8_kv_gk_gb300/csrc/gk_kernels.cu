@@ -139,6 +139,9 @@ __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__
 constexpr int kPlanThreads = 256;
 constexpr int kPlanWarps = kPlanThreads / 32;
 constexpr int kUnitsPerWarp = 8;   // minimum work units per resident warp
+constexpr int kMinPiece = 512;     // shortest piece cut from a chunk for the last wave
+constexpr int kShortSplit = 1024;  // chunks this short ...
+constexpr int kShortMerge = 8;     // ... are not chosen if a row would need more of them
 constexpr int kSplitCands = 22;    // candidate split lengths kMinSplit << k
 constexpr int kRemBuckets = 256;   // remainder size classes for the largest-first order
 
@@ -268,11 +271,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     int k = 0;
     while (k < kSplitCands - 1 && ((long long)kMinSplit << k) < share) ++k;
     while (k > 0 && (s_units[k] + NAct) * planes < kUnitsPerWarp * warps) --k;
+    // no short chunks that would give a row more than kShortMerge partials:
+    // their serial merge outweighs the balance they buy
+    while (k < kSplitCands - 1 && ((long long)kMinSplit << k) <= kShortSplit &&
+           (Lmax - 1) / ((long long)kMinSplit << k) + 1 > kShortMerge)
+      ++k;
     while (k < kSplitCands - 1 && ((long long)kMinSplit << k) * kMaxSplitsPerRow < Lmax) ++k;
     while (k < kSplitCands - 1 && s_need[k] > p.cap) ++k;
     s_S_log = k;
     // Last wave.  Equal chunks give full * planes units of one size; when
-    // that is not a whole number of waves over the warps and the smaller
+    // that is at least one wave but not a whole number of waves over the
+    // warps and the smaller
     // units (remainders, window units) cannot fill the idle part of the last
     // wave, cut the last chunks of the rows with two or more of them into
     // p pieces (largest-first order runs them at the end), keeping whole
@@ -284,12 +293,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     const long long q = cunits / warps, rem = cunits - q * warps;
     const long long gap = (warps - rem) * Sk;                    // idle token slots
     const long long small = (s_remtok[k] + NAct * p.W) * planes;  // work in smaller units
-    if (rem > 0 && small < gap && s_ne[k] > 0) {
+    if (q >= 1 && rem > 0 && small < gap && s_ne[k] > 0) {
       // cv chunks in all, spread over the eligible rows in row order (fewer
       // if a row would pass kMaxSplitsPerRow chunks or the records the
       // workspace holds)
       const long long cv = s_full[k] - (q * warps) / planes;
-      for (int pp = int(min(8ll, Sk / kMinSplit)); pp >= 2; pp >>= 1) {
+      for (int pp = int(min(8ll, Sk / kMinPiece)); pp >= 2; pp >>= 1) {
         const long long per_row = (kMaxSplitsPerRow - 1 - s_maxnf[k]) / (pp - 1);
         const long long room = (p.cap - s_need[k]) / (pp - 1);
         const long long cvp = min(cv, min(per_row * s_ne[k], room));

@@ -103,15 +103,19 @@ def test_split_and_unsplit_agree(name):
     assert gk.gk_read_device_error() == 0
 
 
-@pytest.mark.parametrize("name,step", [("long_cut_small", "split"), ("long_cut_small", "fused")])
-def test_last_wave_pieces(name, step):
-    """Two long rows: equal chunks would leave a partial last wave, so the
-    planner cuts chunks of those rows into pieces that run at the end (header
-    word 7 counts them).  Pieces change only where the splits fall: KV bytes
-    stay bit-exact and the output meets the tolerance, in the two-launch and
-    the single-launch step (whose last piece of each row appends the token)."""
-    w, c, st, cache = _make_cpu(name)
-    ref, kb_ref, vb_ref = tl.oracle_step(w, c, st, cache)
+@pytest.mark.parametrize("step", ["split", "fused"])
+def test_last_wave_pieces(step):
+    """Three long rows over 16 layers: equal chunks would leave a partial last
+    wave, so the planner cuts chunks of those rows into pieces that run at the
+    end (header word 7 counts them).  Pieces change only where the splits
+    fall: every appended KV byte stays bit-exact and sampled outputs meet the
+    tolerance, in the two-launch and the single-launch step (whose last piece
+    or remainder of each row appends the token)."""
+    w = gi.get("long_cut_small")
+    c = gi.make_control(w)
+    st = gi.make_step(w, "cuda")
+    cache = gi.make_cache(w, c, "cuda")
+    pre = [b.clone() for b in cache]
     g = tl.GpuStep(w, c, st, cache)
     if step == "fused":
         g.step()
@@ -122,10 +126,18 @@ def test_last_wave_pieces(name, step):
     assert gk.gk_read_device_error() == 0
     hdr = g.workspace[:256].view(torch.int32).cpu().numpy()
     assert hdr[7] > 0 and hdr[6] > 0, hdr[:8]
-    for j in range(len(g.cache)):
-        assert np.array_equal(g.cache[j][0].cpu().numpy().reshape(-1), kb_ref[j]), ("K", j)
-        assert np.array_equal(g.cache[j][1].cpu().numpy().reshape(-1), vb_ref[j]), ("V", j)
-    tl.check_out(_f64(g.out), _f64(g.out_f32), ref, f"{name}/{step}")
+    kc_d, vc_d = tl.device_appended_codes(g)
+    kc_o, vc_o = tl.oracle_appended_codes(w, c, st)
+    assert np.array_equal(kc_d, kc_o) and np.array_equal(vc_d, vc_o)
+    host = {k: gi.bf16_bits(v) for k, v in st.items()}
+    G = w.num_q_heads // w.num_kv_heads
+    out, of = _f64(g.out), _f64(g.out_f32)
+    for b in range(w.batch):
+        for j in (0, w.num_layers // 2 - 1):
+            res = tl.oracle_row_pair(w, c, host, pre, j, b, kvhs=(0, w.num_kv_heads - 1))
+            for (layer, kvh), ref in res.items():
+                sl = slice(kvh * G, (kvh + 1) * G)
+                tl.check_out(out[layer, b, sl], of[layer, b, sl], ref, f"{step} l{layer} b{b} h{kvh}")
 
 
 def test_repeat_is_bitwise_deterministic():
