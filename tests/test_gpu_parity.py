@@ -140,6 +140,39 @@ def test_last_wave_pieces(step):
                 tl.check_out(out[layer, b, sl], of[layer, b, sl], ref, f"{step} l{layer} b{b} h{kvh}")
 
 
+@pytest.mark.parametrize("name,split_len,pieces", [("gptoss_b1_8k", 1024, False),
+                                                    ("gptoss_b8_8k", 1024, True)])
+def test_plan_choices_at_the_latency_end(name, split_len, pieces):
+    """The planner's choices on 36-layer rows of 8192 tokens, on a GPU with
+    152 SMs (2432 resident warps): chunks of 1024 tokens (512 would give a row
+    16 partials to merge), and chunks cut for the last wave only when the
+    chunks make at least one full wave (8 rows: 3.8 waves; 1 row: 0.5).  The
+    outputs of sampled rows meet the tolerance."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 152:
+        pytest.skip("plan expectations are for 152 SMs")
+    w = gi.get(name)
+    c = gi.make_control(w)
+    st = gi.make_step(w, "cuda")
+    cache = gi.make_cache(w, c, "cuda")
+    pre = [b.clone() for b in cache]
+    g = tl.GpuStep(w, c, st, cache)
+    g.append()
+    g.attention()
+    torch.cuda.synchronize()
+    assert gk.gk_read_device_error() == 0
+    hdr = g.workspace[:256].view(torch.int32).cpu().numpy()
+    assert hdr[4] == split_len and (hdr[7] > 0) == pieces, hdr[:8]
+    host = {k: gi.bf16_bits(v) for k, v in st.items()}
+    G = w.num_q_heads // w.num_kv_heads
+    out, of = _f64(g.out), _f64(g.out_f32)
+    for b in sorted({0, w.batch - 1}):
+        for j in (0, w.num_layers // 2 - 1):
+            res = tl.oracle_row_pair(w, c, host, pre, j, b, kvhs=(0, w.num_kv_heads - 1))
+            for (layer, kvh), ref in res.items():
+                sl = slice(kvh * G, (kvh + 1) * G)
+                tl.check_out(out[layer, b, sl], of[layer, b, sl], ref, f"{name} l{layer} b{b} h{kvh}")
+
+
 def test_repeat_is_bitwise_deterministic():
     w, c, st, cache = _make_cpu("long_small")
     g = tl.GpuStep(w, c, st, cache)
