@@ -183,12 +183,30 @@ def declared_functions() -> list:
     return sorted(set(re.findall(r"\b(gk_[a-z0-9_]+)\s*\(", text)))
 
 
+_variant = None  # a diagnostic build to load instead of libgk.so (use_probe_build)
+
+
+def use_probe_build() -> str:
+    """Load the diagnostic build (per-unit timestamps in the attention kernel,
+    see paged_fp8_kv_gk_gb300.unit_timing) instead of libgk.so.  Must come
+    before the library is first loaded in this process."""
+    global _variant
+    with _lock:
+        if _lib is not None:
+            raise RuntimeError("the library is already loaded")
+        _variant = _build.build_probe()
+    return _variant
+
+
 def lib(build_if_needed: bool = True) -> ctypes.CDLL:
     """Load libgk.so (building it with nvcc first if it is missing or stale)."""
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.build() if build_if_needed else _build.LIB_PATH
+            if _variant is not None:
+                path = _variant
+            else:
+                path = _build.build() if build_if_needed else _build.LIB_PATH
             if not os.path.exists(path):
                 raise RuntimeError(f"{path} is missing: run paged_fp8_kv_gk_gb300.build.build()")
             L = ctypes.CDLL(path)

@@ -16,6 +16,9 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libgk.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
+# the diagnostic build with per-unit timestamps in the attention kernel
+# (GK_PROBE_UNITS=1); never loaded by the product path
+PROBE_LIB_PATH = os.path.join(BUILD_DIR, "probe", "libgk_probe.so")
 ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 
@@ -37,24 +40,27 @@ def _nvcc() -> str:
     return w
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib_path)
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [
         os.path.join(INCLUDE, h) for h in ("gk.h", "gk_testing.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every translation unit and link libgk.so; returns its path."""
-    if not force and not _stale():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, lib_path: str = LIB_PATH,
+          defines: tuple = ()) -> str:
+    """Compile every translation unit and link libgk.so (or, with `defines`,
+    a variant at `lib_path`); returns the library's path."""
+    if not force and not _stale(lib_path):
+        return lib_path
+    out_dir = os.path.dirname(lib_path)
+    os.makedirs(out_dir, exist_ok=True)
     # objects go to a directory of this process's own, so that concurrent
     # builds (parallel test workers) never overwrite each other's files; the
     # library itself is replaced atomically
-    objdir = os.path.join(BUILD_DIR, f"obj{os.getpid()}")
+    objdir = os.path.join(out_dir, f"obj{os.getpid()}")
     os.makedirs(objdir, exist_ok=True)
     nvcc = _nvcc()
     procs = []
@@ -62,7 +68,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     for src in SOURCES:
         obj = os.path.join(objdir, src.replace(".cu", ".o"))
         log = obj + ".log"
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *[f"-D{d}" for d in defines], "-I", INCLUDE, "-c",
+               os.path.join(CSRC, src), "-o", obj]
         f = open(log, "w")
         procs.append((subprocess.Popen(cmd, stdout=f, stderr=subprocess.STDOUT), f, log, cmd))
         objs.append(obj)
@@ -79,14 +86,19 @@ def build(force: bool = False, verbose: bool = False) -> str:
                 sys.stderr.write(text)
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     subprocess.check_call([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"])
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, lib_path)
     for src in SOURCES:  # keep the ptxas reports (registers, spills) beside the library
         log = os.path.join(objdir, src.replace(".cu", ".o.log"))
-        os.replace(log, os.path.join(BUILD_DIR, os.path.basename(log)))
+        os.replace(log, os.path.join(out_dir, os.path.basename(log)))
     shutil.rmtree(objdir, ignore_errors=True)
-    return LIB_PATH
+    return lib_path
+
+
+def build_probe(force: bool = False) -> str:
+    """The diagnostic variant with per-unit timestamps (GK_PROBE_UNITS=1)."""
+    return build(force=force, lib_path=PROBE_LIB_PATH, defines=("GK_PROBE_UNITS=1",))
 
 
 if __name__ == "__main__":
