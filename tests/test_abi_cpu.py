@@ -222,3 +222,17 @@ def test_testing_header_symbol_exported_and_validates():
     assert L.gk_selftest_wait_timeout(10, None, ctypes.byref(b)) == gk.GK_ERR_INVALID_ARG
     assert L.gk_selftest_wait_timeout(10 ** 10, None, ctypes.byref(b)) == gk.GK_ERR_INVALID_ARG
     assert L.gk_selftest_wait_timeout(10 ** 6, None, None) == gk.GK_ERR_INVALID_ARG
+
+
+def test_probe_build_is_separate_from_the_product_library():
+    """The diagnostic unit-timing build is a separate library that can only be
+    chosen before the product library is loaded; the product library exports
+    no timing symbol."""
+    import paged_fp8_kv_gk_gb300.unit_timing as ut
+    from paged_fp8_kv_gk_gb300 import build as gkbuild
+    L = gk.lib()
+    assert not hasattr(L, "gk_probe_units_read")
+    assert gkbuild.PROBE_LIB_PATH != gkbuild.LIB_PATH
+    with pytest.raises(RuntimeError, match="already loaded"):
+        gk.use_probe_build()
+    assert callable(ut.main) and callable(ut.measure)
