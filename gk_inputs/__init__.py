@@ -138,6 +138,11 @@ REDUCED = {
     "max_layers": WORKLOADS["tiny"].replace(
         name="max_layers", num_layers=128, batch=2, block_size=32, lengths="fixed:40,300",
         seed=29, num_blocks=None, scale=None),
+    # forced split lengths: at 512-token chunks these rows take 1, 2, 7 and
+    # 64 chunks (the cap per row; the last row's final chunk holds one key)
+    "split_counts_small": WORKLOADS["gptoss_b64"].replace(
+        name="split_counts_small", num_layers=4, batch=5, lengths="fixed:300,1000,3500,32768,32257",
+        seed=33),
     # DI landing: prompt lengths on both sides of N % B == B - 1 (143, 159 with
     # N >= W; 127 below it), a one-token prompt and block-boundary lengths
     "di_small": WORKLOADS["gptoss_b64"].replace(

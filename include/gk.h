@@ -243,9 +243,12 @@ gk_status gk_decode_step(const gk_shape *shape, const void *q, const void *k_new
  *     GK_STATIC_SCRATCH_BYTES of workspace (gk_attn_workspace_min_bytes); a
  *     smaller array than the recommended workspace only means fewer split-KV
  *     chunks.
- *   - The first call on a device looks up the array's device address with
- *     that device current (cudaGetSymbolAddress) and caches it; make that
- *     first call before any stream capture.
+ *   - Every call looks up the array's device address in the current context
+ *     (cudaGetSymbolAddress, with the caller's device current; no work is
+ *     enqueued), so the address stays right after cudaDeviceReset or in a
+ *     context other than the primary one.  The first call in a context may
+ *     also load the library's device code there: make one call on each device
+ *     before any stream capture.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; each call re-initialises what it needs.  Calls that may overlap
  *     on the GPU (different streams without ordering between them) race on the

@@ -59,3 +59,21 @@ def row_pair_from_pool(w, c, step_host: dict, kpool: np.ndarray, vpool: np.ndarr
             assert st == 0
             res[(layer, kvh)] = out
     return res
+
+
+def row_all_layers(w, c, step_host: dict, gather, b: int, k_layout: int = 0,
+                   sinks=None) -> np.ndarray:
+    """Oracle output of row b for every layer and q head: [NL, Hq, D] float64.
+    gather(b, j) returns the (K pool, V pool) of row b in group buffer j as
+    row_pair_from_pool expects them (from the cache before the append); it is
+    called once per layer pair, so that only one pair's pools are held at a
+    time."""
+    NL, Hq, D, Hkv = w.num_layers, w.num_q_heads, w.head_dim, w.num_kv_heads
+    G = Hq // Hkv
+    out = np.zeros((NL, Hq, D), np.float64)
+    for j in range(NL // 2):
+        kp, vp = gather(b, j)
+        res = row_pair_from_pool(w, c, step_host, kp, vp, j, b, None, k_layout, sinks)
+        for (layer, kvh), o in res.items():
+            out[layer, kvh * G:(kvh + 1) * G] = o
+    return out

@@ -183,30 +183,12 @@ def declared_functions() -> list:
     return sorted(set(re.findall(r"\b(gk_[a-z0-9_]+)\s*\(", text)))
 
 
-_variant = None  # a diagnostic build to load instead of libgk.so (use_probe_build)
-
-
-def use_probe_build() -> str:
-    """Load the diagnostic build (per-unit timestamps in the attention kernel,
-    see paged_fp8_kv_gk_gb300.unit_timing) instead of libgk.so.  Must come
-    before the library is first loaded in this process."""
-    global _variant
-    with _lock:
-        if _lib is not None:
-            raise RuntimeError("the library is already loaded")
-        _variant = _build.build_probe()
-    return _variant
-
-
 def lib(build_if_needed: bool = True) -> ctypes.CDLL:
     """Load libgk.so (building it with nvcc first if it is missing or stale)."""
     global _lib
     with _lock:
         if _lib is None:
-            if _variant is not None:
-                path = _variant
-            else:
-                path = _build.build() if build_if_needed else _build.LIB_PATH
+            path = _build.build() if build_if_needed else _build.LIB_PATH
             if not os.path.exists(path):
                 raise RuntimeError(f"{path} is missing: run paged_fp8_kv_gk_gb300.build.build()")
             L = ctypes.CDLL(path)
@@ -245,6 +227,8 @@ def lib(build_if_needed: bool = True) -> ctypes.CDLL:
             L.gk_selftest_wait_timeout.restype = ctypes.c_int
             L.gk_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp,
                                                    ctypes.POINTER(ctypes.c_uint32)]
+            L.gk_selftest_decode_attn_split.restype = ctypes.c_int
+            L.gk_selftest_decode_attn_split.argtypes = [sp] + [vp] * 15 + [sz, i32, vp]
             L.gk_read_device_error.restype = ctypes.c_int
             L.gk_read_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
             _lib = L
@@ -504,6 +488,26 @@ def gk_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     if st not in (GK_OK, GK_ERR_DEVICE_BOUNDS):
         raise GkError(st, "gk_selftest_wait_timeout")
     return int(bits.value)
+
+
+def gk_selftest_decode_attn_split(shape, q, kv: KvCache, k_scale, v_scale, cos, sin, bt_full,
+                                  bt_swa, pos, pos_w, active, out, out_f32, workspace,
+                                  split_tokens: int, stream=None, sinks=None) -> None:
+    """Test hook (include/gk_testing.h): gk_decode_attn_stack with the split-KV
+    chunk length fixed to `split_tokens` (a power of two >= 512)."""
+    import torch
+    sh = _as_shape(shape)
+    st = lib().gk_selftest_decode_attn_split(
+        ctypes.byref(sh), _ptr(q, torch.bfloat16, "q"), _kv(kv, sh),
+        _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
+        _ptr(cos, torch.float32, "cos"), _ptr(sin, torch.float32, "sin"),
+        _ptr(bt_full, torch.int32, "bt_full"), _ptr(bt_swa, torch.int32, "bt_swa"),
+        _ptr(pos, torch.int32, "pos"), _ptr(pos_w, torch.int32, "pos_w"),
+        _ptr(active, torch.uint8, "active"), _sinks(sinks, sh), _ptr(out, torch.bfloat16, "out"),
+        _ptr(out_f32, torch.float32, "out_f32", allow_none=True),
+        _ptr(workspace, torch.uint8, "workspace"), int(workspace.numel()), int(split_tokens),
+        _stream(stream, q))
+    _check(st, "gk_selftest_decode_attn_split")
 
 
 def new_workspace(shape, device="cuda"):

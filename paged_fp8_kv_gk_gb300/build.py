@@ -16,9 +16,6 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libgk.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
-# the diagnostic build with per-unit timestamps in the attention kernel
-# (GK_PROBE_UNITS=1); never loaded by the product path
-PROBE_LIB_PATH = os.path.join(BUILD_DIR, "probe", "libgk_probe.so")
 ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 
@@ -94,11 +91,6 @@ def build(force: bool = False, verbose: bool = False, lib_path: str = LIB_PATH,
         os.replace(log, os.path.join(out_dir, os.path.basename(log)))
     shutil.rmtree(objdir, ignore_errors=True)
     return lib_path
-
-
-def build_probe(force: bool = False) -> str:
-    """The diagnostic variant with per-unit timestamps (GK_PROBE_UNITS=1)."""
-    return build(force=force, lib_path=PROBE_LIB_PATH, defines=("GK_PROBE_UNITS=1",))
 
 
 if __name__ == "__main__":

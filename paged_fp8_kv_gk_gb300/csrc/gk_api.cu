@@ -205,7 +205,7 @@ static gk_status decode_attention(const gk_shape* shape, const void* q, const gk
                                   const int32_t* bt_swa, const int32_t* pos, const int32_t* pos_w,
                                   const uint8_t* active, const float* sinks, void* out,
                                   float* out_f32, void* workspace, size_t ws_bytes, void* stream,
-                                  const AppendInputs* app) {
+                                  const AppendInputs* app, int force_split_log = -1) {
   gk_status st = check_shape(shape);
   if (st != GK_OK) return st;
   if (!q || !k_scale || !v_scale || !cos || !sin || !bt_full || !bt_swa ||
@@ -290,6 +290,7 @@ static gk_status decode_attention(const gk_shape* shape, const void* q, const gk
   pl.W = shape->window;
   pl.max_tokens_full = shape->max_blocks_full * shape->block_size;
   pl.max_tokens_swa = shape->max_blocks_swa * shape->block_size;
+  pl.force_split_log = force_split_log;
   return launch_attention(pl, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GK_OK
                                                                                    : GK_ERR_CUDA;
 }
@@ -441,6 +442,22 @@ gk_status gk_e4m3_quantize(const float* x, float scale, uint8_t* codes, int64_t 
   return launch_quantize(x, scale, codes, n, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? GK_OK
              : GK_ERR_CUDA;
+}
+
+gk_status gk_selftest_decode_attn_split(const gk_shape* shape, const void* q,
+                                        const gk_kv_cache* kv, const float* k_scale,
+                                        const float* v_scale, const float* cos, const float* sin,
+                                        const int32_t* bt_full, const int32_t* bt_swa,
+                                        const int32_t* pos, const int32_t* pos_w,
+                                        const uint8_t* active, const float* sinks, void* out,
+                                        float* out_f32, void* workspace, size_t ws_bytes,
+                                        int32_t split_tokens, void* stream) {
+  int k = -1;
+  for (int c = 0; c < 22; ++c)
+    if ((kMinSplit << c) == split_tokens) k = c;
+  if (k < 0) return GK_ERR_INVALID_ARG;
+  return decode_attention(shape, q, kv, k_scale, v_scale, cos, sin, bt_full, bt_swa, pos, pos_w,
+                          active, sinks, out, out_f32, workspace, ws_bytes, stream, nullptr, k);
 }
 
 gk_status gk_selftest_wait_timeout(uint64_t limit_ns, void* stream, uint32_t* bits) {

@@ -90,6 +90,10 @@ struct PlanParams {
   int64_t cap;
   int NL, Bt, Hkv, W, n_warps;
   int max_tokens_full, max_tokens_swa;  // table row lengths in tokens
+  // test hook: split length kMinSplit << force_split_log (-1: the planner's
+  // choice), still raised if a row would need more than kMaxSplitsPerRow
+  // chunks or the records would not fit; no last-wave pieces
+  int force_split_log;
 };
 
 struct AttnParams {

@@ -162,18 +162,6 @@ __device__ __forceinline__ long long warp_sum64(long long v) {
 // u % planes of entry u / planes.  Full-layer entries come first, largest
 // first; then one sliding-window entry per active row; then zero-fill units
 // (one per inactive row and layer).
-// Unit timing (diagnostic build only, GK_PROBE_UNITS=1): each warp stamps its
-// start and, for each of its first kProbeUnits units, when it began waiting for
-// the unit's first stage, when the epilogue ended, the time spent waiting on
-// stage barriers and the unit's shape.  The product build compiles none of it.
-#ifndef GK_PROBE_UNITS
-#define GK_PROBE_UNITS 0
-#endif
-#if GK_PROBE_UNITS
-constexpr int kProbeWarps = 4096, kProbeUnits = 64;
-__device__ unsigned long long g_probe_units[size_t(kProbeWarps) * kProbeUnits * 4];
-__device__ unsigned long long g_probe_warps[kProbeWarps * 2];
-#endif
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams p) {
   // let the attention grid launch now; it waits for this grid before reading the plan
@@ -289,6 +277,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     while (k < kSplitCands - 1 && ((long long)kMinSplit << k) <= kShortSplit &&
            (Lmax - 1) / ((long long)kMinSplit << k) + 1 > kShortMerge)
       ++k;
+    if (p.force_split_log >= 0) k = p.force_split_log;  // test hook: a fixed split length
     while (k < kSplitCands - 1 && ((long long)kMinSplit << k) * kMaxSplitsPerRow < Lmax) ++k;
     while (k < kSplitCands - 1 && s_need[k] > p.cap) ++k;
     s_S_log = k;
@@ -306,7 +295,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     const long long q = cunits / warps, rem = cunits - q * warps;
     const long long gap = (warps - rem) * Sk;                    // idle token slots
     const long long small = (s_remtok[k] + NAct * p.W) * planes;  // work in smaller units
-    if (q >= 1 && rem > 0 && small < gap && s_ne[k] > 0) {
+    if (p.force_split_log < 0 && q >= 1 && rem > 0 && small < gap && s_ne[k] > 0) {
       // cv chunks in all, spread over the eligible rows in row order (fewer
       // if a row would pass kMaxSplitsPerRow chunks or the records the
       // workspace holds)
@@ -683,12 +672,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
 
   // the planner grid (launched just before) must be complete from here on
   asm volatile("griddepcontrol.wait;" ::: "memory");
-#if GK_PROBE_UNITS
-  const int probe_w = blockIdx.x * kWarps + warp;
-  unsigned long long probe_t0 = 0, probe_wait = 0;
-  int probe_n = 0;
-  if (lane == 0 && probe_w < kProbeWarps) g_probe_warps[2 * probe_w] = globaltimer_ns();
-#endif
   const int nU = p.hdr[kHdrNUnits];
   const int nAll = nU + p.hdr[kHdrNZero];  // units with a descriptor, then zero-fill units
 
@@ -939,18 +922,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     const int slot = c_slot;
     const uint32_t bar = bar0 + 8 * slot;
     const uint32_t parity = c_par;
-#if GK_PROBE_UNITS
-    const unsigned long long probe_a = globaltimer_ns();
-#endif
     if (!mbar_wait_bounded(bar, parity, kWaitLimitNs)) failed = true;
-#if GK_PROBE_UNITS
-    const unsigned long long probe_b = globaltimer_ns();
-    if (k_in_unit == 0) {
-      probe_t0 = probe_a;
-      probe_wait = 0;
-    }
-    probe_wait += probe_b - probe_a;
-#endif
     if (__any_sync(kFull, failed)) {
       failed = true;
       break;
@@ -1430,23 +1402,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
           }
         }
       }
-#if GK_PROBE_UNITS
-      if (lane == 0 && probe_w < kProbeWarps && probe_n < kProbeUnits) {
-        unsigned long long* r = g_probe_units + (size_t(probe_w) * kProbeUnits + probe_n) * 4;
-        r[0] = probe_t0;
-        r[1] = globaltimer_ns();
-        r[2] = probe_wait;
-        r[3] = (unsigned long long)(cd.n_st | (CU.kind << 16) | (CU.ns << 20)) |
-               ((unsigned long long)(cd.t_end - cd.t_begin) << 32);
-      }
-      ++probe_n;
-#endif
       ++f_head;
     }
   }
-#if GK_PROBE_UNITS
-  if (lane == 0 && probe_w < kProbeWarps) g_probe_warps[2 * probe_w + 1] = probe_n;
-#endif
 
 #undef CU
   if (failed) {
@@ -1461,17 +1419,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   }
 }
 
-#if GK_PROBE_UNITS
-// Copies the unit-timing arrays to host memory (diagnostic build only).
-extern "C" __attribute__((visibility("default"))) int gk_probe_units_read(
-    void* units, size_t units_bytes, void* warps, size_t warps_bytes) {
-  cudaError_t e = cudaMemcpyFromSymbol(
-      units, g_probe_units, units_bytes < sizeof(g_probe_units) ? units_bytes : sizeof(g_probe_units));
-  if (e != cudaSuccess) return int(e);
-  return int(cudaMemcpyFromSymbol(
-      warps, g_probe_warps, warps_bytes < sizeof(g_probe_warps) ? warps_bytes : sizeof(g_probe_warps)));
-}
-#endif
 
 // =========================================================================
 // Test hook: the bounded barrier wait running out

@@ -15,32 +15,25 @@
 // workspace.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "gk_internal.h"
 
 namespace {
 
 static __device__ __align__(256) uint8_t g_gk_static_scratch[GK_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device.  In host code
+// Device address of the scratch array in the current context.  In host code
 // g_gk_static_scratch names a host-side stand-in, not device memory, so the
-// address is looked up once per device (with that device current) and cached.
+// address is looked up on every call, with the caller's device current: the
+// lookup is cheap, enqueues no work, and stays right when the module is loaded
+// again at another address (after cudaDeviceReset, or in another context on
+// the same device).
 gk_status static_scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GK_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_gk_static_scratch) != cudaSuccess || p == nullptr)
-      return GK_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_gk_static_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return GK_ERR_CUDA;
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return GK_OK;
 }
 

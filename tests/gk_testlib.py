@@ -12,6 +12,8 @@ Tolerances (written here once, used by every parity test):
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -31,7 +33,10 @@ def ulp_bf16(x: np.ndarray) -> np.ndarray:
 
 
 def check_out(out_bf16: np.ndarray, out_f32, ref: np.ndarray, what: str = ""):
-    """out_bf16: float64 view of the kernel's bf16 output; out_f32 may be None."""
+    """out_bf16: float64 view of the kernel's bf16 output; out_f32 may be None.
+    Returns the error statistics, with `bf16_widened`: how many bf16 elements
+    differ from the oracle by more than MAX_ABS and pass only because one bf16
+    step of the value is larger than MAX_ABS."""
     d = np.abs(out_bf16 - ref)
     lim = np.maximum(MAX_ABS, ulp_bf16(ref))
     bad = d > lim
@@ -39,13 +44,15 @@ def check_out(out_bf16: np.ndarray, out_f32, ref: np.ndarray, what: str = ""):
                            ref[bad][:5].tolist(), out_bf16[bad][:5].tolist())
     mean_r = float(np.mean(np.abs(out_bf16 - oracle.round_bf16(ref)))) if ref.size else 0.0
     assert mean_r <= MEAN_ABS, (what, "bf16 mean", mean_r)
-    stats = {"bf16_max": float(d.max()) if d.size else 0.0, "bf16_mean_vs_rne": mean_r}
+    stats = {"bf16_max": float(d.max()) if d.size else 0.0, "bf16_mean_vs_rne": mean_r,
+             "bf16_widened": int(np.count_nonzero(d > MAX_ABS)), "elements": int(d.size)}
     if out_f32 is not None:
         e = np.abs(out_f32 - ref)
         assert e.max() <= MAX_ABS, (what, "f32 max", float(e.max()))
         assert e.mean() <= MEAN_ABS, (what, "f32 mean", float(e.mean()))
         stats.update(f32_max=float(e.max()), f32_mean=float(e.mean()))
-    print("check_out", what, {k: round(v, 6) for k, v in stats.items()})
+    print("check_out", what, {k: (round(v, 6) if isinstance(v, float) else v)
+                              for k, v in stats.items()})
     return stats
 
 
@@ -211,3 +218,38 @@ def device_appended_codes(g: GpuStep):
                          g.k_layout).cpu().numpy()
         vc[i] = vview[pb[:, None], hk[None, :], t[:, None], :].cpu().numpy()
     return kc, vc
+
+
+def host_threads() -> int:
+    """Host threads for the oracle: the cores this process may use."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def oracle_full_output(w: gi.Workload, c: gi.Control, step_host: dict, pre_cache,
+                       k_layout: int = 0, sinks=None, threads: int = None) -> np.ndarray:
+    """The oracle's output for every (layer, row, q head) of a workload of any
+    size: [NL, Bt, Hq, D] float64, zero on inactive rows.  Each active row is
+    one task (every layer pair, every kv head; oracle.rows.row_all_layers) on
+    a pool of host threads (the oracle's C calls release the GIL); a task
+    copies its row's blocks from `pre_cache` (the device cache before the
+    append) one layer pair at a time.  step_host: q, k_new, v_new as uint16
+    bf16 bit arrays."""
+    from concurrent.futures import ThreadPoolExecutor
+    NL, Bt, Hq, D = w.num_layers, w.batch, w.num_q_heads, w.head_dim
+    ref = np.zeros((NL, Bt, Hq, D), np.float64)
+    gather = lambda b, j: gather_row_pool(w, c, pre_cache, j, b)  # noqa: E731
+
+    def task(b):
+        ref[:, b] = oracle_rows.row_all_layers(w, c, step_host, gather, b, k_layout, sinks)
+        return b
+
+    rows = [int(b) for b in np.nonzero(c.active)[0]]
+    # longest rows first, so that the pool's last tasks are short ones
+    rows.sort(key=lambda b: -int(c.lengths[b]))
+    with ThreadPoolExecutor(max_workers=threads or host_threads()) as ex:
+        done = list(ex.map(task, rows))
+    assert len(done) == len(rows)
+    return ref

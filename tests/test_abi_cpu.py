@@ -224,15 +224,18 @@ def test_testing_header_symbol_exported_and_validates():
     assert L.gk_selftest_wait_timeout(10 ** 6, None, None) == gk.GK_ERR_INVALID_ARG
 
 
-def test_probe_build_is_separate_from_the_product_library():
-    """The diagnostic unit-timing build is a separate library that can only be
-    chosen before the product library is loaded; the product library exports
-    no timing symbol."""
-    import paged_fp8_kv_gk_gb300.unit_timing as ut
-    from paged_fp8_kv_gk_gb300 import build as gkbuild
+@no_device
+def test_split_hook_exported_and_validates_the_length():
+    """gk_selftest_decode_attn_split (include/gk_testing.h) refuses a split
+    length that is not a power of two from 512 to 512 << 21 before anything
+    else is looked at."""
     L = gk.lib()
-    assert not hasattr(L, "gk_probe_units_read")
-    assert gkbuild.PROBE_LIB_PATH != gkbuild.LIB_PATH
-    with pytest.raises(RuntimeError, match="already loaded"):
-        gk.use_probe_build()
-    assert callable(ut.main) and callable(ut.measure)
+    sh = gk.Shape.make(num_layers=4, batch=5, num_q_heads=64, num_kv_heads=8, head_dim=64,
+                       block_size=32, num_blocks=4096, window=128, max_blocks_full=1024,
+                       max_blocks_swa=5)
+    kvs, arrs = _kv_struct()
+    for bad in (0, -512, 256, 513, 1000, 3 << 9, 512 << 22):
+        st = L.gk_selftest_decode_attn_split(ctypes.byref(sh), FAKE, ctypes.byref(kvs),
+                                             *([FAKE] * 9), None, FAKE, None, FAKE, 1 << 30, bad,
+                                             None)
+        assert st == gk.GK_ERR_INVALID_ARG, bad

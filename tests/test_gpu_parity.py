@@ -300,6 +300,11 @@ def _kv_untouched(g, pre, c, w):
 
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_parity(name):
+    """A full-size workload in the benchmark's launch configuration
+    (recommended workspace, persistent grid): every appended KV byte
+    bit-exact, every other cache byte unchanged, and every output element of
+    every (layer, row, q head) against the oracle, the whole output computed
+    by the oracle row by row on the host cores."""
     w = gi.get(name)
     c = gi.make_control(w)
     st = gi.make_step(w, "cuda")
@@ -319,27 +324,16 @@ def test_full_size_parity(name):
     assert np.array_equal(vc_d[:, act], vc_o[:, act])
     _kv_untouched(g, pre, c, w)
 
-    # properties over the whole output
-    assert torch.isfinite(g.out_f32).all()
-    assert (g.out[:, torch.as_tensor(~act, device="cuda")] == 0).all()
-
-    # sampled rows through the oracle
-    host = {k: gi.bf16_bits(v) for k, v in st.items()}
-    rng = np.random.default_rng(101)
-    actives = np.nonzero(act)[0]
-    L = c.lengths
-    rows = {int(actives[np.argmax(L[actives])]), int(actives[np.argmin(L[actives])])}
-    rows |= set(int(x) for x in rng.choice(actives, size=min(2, actives.size), replace=False))
-    G = w.num_q_heads // w.num_kv_heads
-    js = sorted({0, w.num_layers // 2 - 1, int(rng.integers(0, w.num_layers // 2))})
+    # the whole output against the oracle
     out = g.out.float().cpu().numpy().astype(np.float64)
     of = g.out_f32.cpu().numpy().astype(np.float64)
-    for b in sorted(rows):
-        for j in js:
-            res = tl.oracle_row_pair(w, c, host, pre, j, b, kvhs=(0, w.num_kv_heads - 1))
-            for (layer, kvh), ref in res.items():
-                sl = slice(kvh * G, (kvh + 1) * G)
-                tl.check_out(out[layer, b, sl], of[layer, b, sl], ref, f"{name} l{layer} b{b} h{kvh}")
+    del g, cache
+    host = {k: gi.bf16_bits(v) for k, v in st.items()}
+    ref = tl.oracle_full_output(w, c, host, pre)
+    assert (out[:, ~act] == 0).all() and (of[:, ~act] == 0).all()
+    stats = tl.check_out(out, of, ref, f"{name} whole output")
+    print(f"{name}: {stats['elements']} elements compared, {stats['bf16_widened']} bf16 elements "
+          f"within one bf16 step but beyond {tl.MAX_ABS}")
 
 
 def test_full_size_repeat_bitwise():

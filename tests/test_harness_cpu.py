@@ -25,6 +25,21 @@ def test_row_pair_sampler_equals_whole_step(name):
                 assert np.array_equal(o, full[layer, b, kvh * G:(kvh + 1) * G]), (b, layer, kvh)
 
 
+@pytest.mark.parametrize("name", ["tiny", "ragged_small", "swa_small", "gk120b_rank_small"])
+def test_threaded_whole_output_equals_whole_step(name):
+    """The whole-output oracle used at full size (rows on host threads, blocks
+    copied one layer pair at a time) gives exactly the whole-step oracle's
+    output, zeros on inactive rows included."""
+    w = gi.get(name)
+    c = gi.make_control(w)
+    st = gi.make_step(w, "cpu")
+    cache = gi.make_cache(w, c, "cpu")
+    full, _, _ = tl.oracle_step(w, c, st, cache)
+    host = {k: gi.bf16_bits(v) for k, v in st.items()}
+    got = tl.oracle_full_output(w, c, host, cache, threads=3)
+    assert np.array_equal(got, full)
+
+
 @pytest.mark.parametrize("name", ["tiny", "ragged_small", "swa_small_sat"])
 def test_appended_codes_helper_equals_whole_buffer_append(name):
     w = gi.get(name)

@@ -4,10 +4,12 @@ first step, a plugin boundary without a device allocator, a step that must not
 risk cudaMalloc's synchronisation or failure).  It runs on the library's own
 fixed scratch array instead of a caller workspace.
 
-Checked through the C ABI against the workspace entry point on the same
-inputs, on two calls in a row (the second call reuses the array the first one
-left behind), within the parity tests' tolerance.  Works alone in a fresh
-process and after the other tests.
+Checked through the C ABI against the workspace entry point and against the
+oracle on the same inputs, on two calls in a row (the second call reuses the
+array the first one left behind), within the parity tests' tolerance; and once
+at the 36-layer batch-64 size, where the fixed array holds fewer split-KV
+records than the recommended workspace, against the oracle on every output
+element.  Works alone in a fresh process and after the other tests.
 """
 import ctypes
 
@@ -40,6 +42,7 @@ def test_static_scratch_matches_workspace_entry_point(name):
     c = gi.make_control(w)
     st = gi.make_step(w, "cpu")
     cache = gi.make_cache(w, c, "cpu")
+    ora, _, _ = tl.oracle_step(w, c, st, cache)
     g = tl.GpuStep(w, c, st, cache)
     g.append()
     g.attention()                       # existing entry point, caller workspace
@@ -53,7 +56,34 @@ def test_static_scratch_matches_workspace_entry_point(name):
                                        out_f32)
         torch.cuda.synchronize()
         assert gk.gk_read_device_error() == 0
-        tl.check_out(_f64(out), _f64(out_f32), ref, f"{name} static call {call}")
+        tl.check_out(_f64(out), _f64(out_f32), ref, f"{name} static call {call} vs workspace")
+        tl.check_out(_f64(out), _f64(out_f32), ora, f"{name} static call {call} vs oracle")
+
+
+def test_static_scratch_full_size_against_the_oracle():
+    """36 layers, batch 64, contexts U{1024..8192}: the recommended workspace
+    is larger than the fixed array, so the planner runs with fewer split-KV
+    records than it would choose (longer chunks); every output element still
+    meets the tolerance against the oracle."""
+    w = gi.get("gptoss_b64")
+    c = gi.make_control(w)
+    st = gi.make_step(w, "cuda")
+    cache = gi.make_cache(w, c, "cuda")
+    pre = [b.clone() for b in cache]
+    g = tl.GpuStep(w, c, st, cache)
+    assert gk.gk_attn_workspace_bytes(g.shape) > (16 << 20) >= gk.gk_attn_workspace_min_bytes(g.shape)
+    g.append()
+    out = torch.full_like(g.out, float("nan"))
+    out_f32 = torch.full_like(g.out_f32, float("nan"))
+    gk.gk_decode_attn_stack_static(g.shape, g.q, g.kv, g.k_scale, g.v_scale, g.cos, g.sin,
+                                   g.bt_full, g.bt_swa, g.pos, g.pos_w, g.active, out, out_f32)
+    torch.cuda.synchronize()
+    assert gk.gk_read_device_error() == 0
+    o, of = _f64(out), _f64(out_f32)
+    del g, cache, out, out_f32
+    host = {k: gi.bf16_bits(v) for k, v in st.items()}
+    ref = tl.oracle_full_output(w, c, host, pre)
+    tl.check_out(o, of, ref, "gptoss_b64 static whole output")
 
 
 def test_static_scratch_rejects_shapes_beyond_its_size():
