@@ -14,10 +14,15 @@ inputs copied from pinned host memory and the output copied back inside the
 timed region; `roofline` is for the attention call (planner + persistent
 kernel): algorithmic bytes (KV bytes the step must read, counted exactly from
 the context lengths, plus q and out) / its CUDA-event duration, against the
-measured HBM copy bandwidth.  `--impl reference` times the oracle (plain C,
-one thread) on a bounded sample of the same workload.
-Multi-GPU (torchrun): every rank runs an independent replica (no collective
-on the data path); the timing is barrier-bracketed and the max over ranks.
+measured HBM copy bandwidth.  On the default workload at one GPU the line also
+carries `per_config`: the same figures for every other workload of the
+measurement, each timed in the same run.  `--impl reference` times the oracle
+(plain C) on whole rows of the same workload on the host cores.
+Multi-GPU: `--gpus N` starts N replicas itself (torch.distributed.run, one
+process per GPU) unless it already runs under a launcher with WORLD_SIZE = N.
+Every rank runs an independent replica (no collective on the data path, no
+NCCL); the timing reduction (max over ranks of the elapsed time, sum of the
+units) goes through a gloo group on the host.
 """
 from __future__ import annotations
 
@@ -51,7 +56,7 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
 
 
-def dist_init(backend: str):
+def dist_init(backend: str = "gloo"):
     import torch.distributed as dist
     rank, _, ws = dist_env()
     if ws > 1 and not dist.is_initialized():
@@ -60,15 +65,36 @@ def dist_init(backend: str):
 
 
 def reduce_timing(local_ms: float, local_units: float, dist=None, device=None):
-    """(max elapsed ms over ranks, total units over ranks)."""
+    """(max elapsed ms over ranks, total units over ranks), on the host (gloo)."""
     if dist is None:
         return local_ms, local_units
     import torch
-    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
-    u = torch.tensor([local_units], dtype=torch.float64, device=device)
+    t = torch.tensor([local_ms], dtype=torch.float64)
+    u = torch.tensor([local_units], dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     dist.all_reduce(u, op=dist.ReduceOp.SUM)
     return float(t.item()), float(u.item())
+
+
+def launch_replicas(gpus: int, argv) -> int:
+    """--gpus N outside a launcher: run this script as N ranks on this node
+    (torch.distributed.run, rendezvous on 127.0.0.1) and return its exit code;
+    None when this process is already a rank (WORLD_SIZE set) or N == 1."""
+    if "WORLD_SIZE" in os.environ:
+        ws = int(os.environ["WORLD_SIZE"])
+        if ws != gpus:
+            raise SystemExit(f"--gpus {gpus} but WORLD_SIZE={ws}: launch one rank per GPU")
+        return None
+    if gpus == 1:
+        return None
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={gpus}", "--master-addr", "127.0.0.1", f"--master-port={port}",
+           os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
 
 
 # ------------------------------------------------------------------ helpers
@@ -89,25 +115,48 @@ def attn_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per attention launch from a committed ncu summary, if it was
-    taken on the current kernel source; else None."""
+# DRAM traffic of the attention kernel is captured on a reduced case of each
+# workload (same per-row shape, a few GB of KV, larger than L2) and scaled to
+# the full workload by the ratio of algorithmic bytes per launch.
+TRAFFIC_CASES = {"gptoss_b64": "gptoss_b16", "swa_b512": "swa_b128", "long_ctx": "long_b1",
+                 "ragged_b256": "ragged_b24", "gk120b_rank_b64": "gk120b_rank_b64"}
+
+
+def traffic_command(case: str) -> str:
+    return ("ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum "
+            "--clock-control none -k regex:attn_kernel -s 3 -c 3 --csv --log-file launches.csv "
+            f"python bench.py --workload {case} --steps 3 --warmup 3 --no-cpu-baseline "
+            "--no-per-config")
+
+
+def alg_bytes(w, c) -> int:
+    """Algorithmic bytes of one attention launch: KV read (exact) + q + out."""
+    return gi.kv_bytes_read(w, c) + gi.qo_bytes(w, c)
+
+
+def recorded_traffic(w, c):
+    """DRAM bytes per attention launch of workload w, from the committed ncu
+    capture of its reduced case scaled by algorithmic bytes, if that capture
+    was taken on the current kernel source; else None.  Returns
+    (bytes, reduced case, scale)."""
     p = os.path.join(ROOT, "profiles", "attn_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    e = d.get(workload)
+    case = TRAFFIC_CASES.get(w.name, w.name)
+    e = d.get(case)
     if not e or e.get("kernel_src_sha") != attn_source_hash():
         return None
-    return e.get("dram_bytes_per_launch")
+    scale = alg_bytes(w, c) / e["alg_bytes_per_launch"]
+    return int(round(e["dram_bytes_per_launch"] * scale)), case, scale
 
 
-def record_traffic(workload: str, csv_path: str, out_path: str = None) -> dict:
-    """Average DRAM bytes per attention launch from an ncu launch list (the
-    `--metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum
-    --csv` output of a run of this bench on `workload`) into
-    profiles/attn_traffic.json, stamped with the current kernel source hash."""
+def record_traffic(case: str, csv_path: str, out_path: str = None) -> dict:
+    """Average DRAM bytes per attention launch from an ncu launch list of this
+    bench on the reduced case `case` (traffic_command(case)) into
+    profiles/attn_traffic.json, with the case's algorithmic bytes per launch
+    and the current kernel source hash."""
     import csv
     vals = {}
     with open(csv_path) as f:
@@ -120,24 +169,116 @@ def record_traffic(workload: str, csv_path: str, out_path: str = None) -> dict:
         vals.setdefault(r[hdr["Metric Name"]], []).append(v)
     rd = statistics.fmean(vals["dram__bytes_read.sum"])
     wr = statistics.fmean(vals["dram__bytes_write.sum"])
+    w = gi.get(case)
+    c = gi.make_control(w)
     entry = {"kernel_src_sha": attn_source_hash(), "dram_bytes_per_launch": int(rd + wr),
              "dram_read_bytes": int(rd), "dram_write_bytes": int(wr),
+             "alg_bytes_per_launch": alg_bytes(w, c),
              "launches_averaged": len(vals["dram__bytes_read.sum"]),
              "avg_launch_ns_under_ncu": round(statistics.fmean(vals["gpu__time_duration.sum"]), 1),
-             "command": "ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,"
-                        "dram__bytes_write.sum --clock-control none -k regex:\"attn_kernel|"
-                        "plan_kernel|kv_append_kernel\" --csv --log-file launches.csv python "
-                        f"bench.py --workload {workload} --steps 3 --warmup 3 --no-cpu-baseline"}
+             "command": traffic_command(case)}
     p = out_path or os.path.join(ROOT, "profiles", "attn_traffic.json")
     d = {}
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-    d[workload] = entry
+    d[case] = entry
     with open(p, "w") as f:
         json.dump(d, f, indent=1)
         f.write("\n")
     return entry
+
+
+def device_selector(dev) -> str:
+    """The GPU of torch device `dev` as nvidia-smi / NVML name it (UUID, else
+    PCI bus id; NVML ignores CUDA_VISIBLE_DEVICES, so an index would not do)."""
+    import torch
+    pr = torch.cuda.get_device_properties(dev)
+    u = getattr(pr, "uuid", None)
+    if u is not None:
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    if hasattr(pr, "pci_bus_id"):
+        return f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+    return str(dev.index or 0)
+
+
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons read through NVML (the driver's
+    libnvidia-ml, read-only queries) every `period_s` on a host thread; only
+    the samples taken between mark_begin and mark_end count.  Fine enough to
+    put several samples inside a timed region of a few milliseconds."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, selector: str, period_s: float = 0.002):
+        import ctypes
+        import threading
+        self.period = period_s
+        self.rows = []
+        self.t0 = self.t1 = None
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        if L.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.L = L
+        self.h = ctypes.c_void_p()
+        if selector.startswith("GPU-"):
+            rc = L.nvmlDeviceGetHandleByUUID(selector.encode(), ctypes.byref(self.h))
+        else:
+            rc = L.nvmlDeviceGetHandleByPciBusId_v2(selector.encode(), ctypes.byref(self.h))
+        if rc != 0:
+            raise OSError(f"no NVML handle for {selector}")
+        self.reasons_fn = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            L.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        L.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
+        self.stop_ev = threading.Event()
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+
+    def _loop(self):
+        import ctypes
+        clk, rs, pw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+        while not self.stop_ev.is_set():
+            t = time.perf_counter()
+            self.L.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk))
+            self.reasons_fn(self.h, ctypes.byref(rs))
+            self.L.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(pw))
+            self.rows.append((t, float(clk.value), int(rs.value), pw.value / 1000.0))
+            time.sleep(self.period)
+
+    def start(self):
+        self.thread.start()
+        time.sleep(0.05)
+
+    def mark_begin(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
+
+    def stop(self):
+        time.sleep(0.02)
+        self.stop_ev.set()
+        self.thread.join(timeout=5)
+        self.L.nvmlShutdown()
+        inside = [r for r in self.rows if self.t0 is not None and self.t0 <= r[0] <= (self.t1 or r[0])]
+        use = inside if inside else self.rows
+        if not use:
+            return None
+        reasons = sorted({n for r in use for bit, n in self.REASONS.items() if r[2] & bit})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": self.max_mhz,
+                "samples": len(self.rows), "samples_in_timed_region": len(inside),
+                "power_w_max": max(r[3] for r in use), "reasons": reasons, "source": "nvml"}
+
+
+def clock_sampler(dev):
+    """NVML sampler for the GPU of `dev`, else the nvidia-smi one."""
+    sel = device_selector(dev)
+    try:
+        return NvmlClockSampler(sel)
+    except (OSError, AttributeError):
+        return ClockSampler(sel)
 
 
 class ClockSampler:
@@ -147,7 +288,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index):
         self.index = index
         self.proc = None
         self.path = None
@@ -214,14 +355,13 @@ def kv_layout_desc(k_layout: str = "packed", kv_form: str = "per_group") -> str:
     return f"{form}, {k}, E4M3"
 
 
-def workload_config(w, c, l2_note: str, kv_layout: str = None):
+def workload_config(w, c, kv_layout: str = None):
     kind, _, arg = w.lengths.partition(":")
     return {"workload": w.name, "num_layers": w.num_layers, "batch": w.batch,
             "active_rows": int(c.active.sum()), "q_heads": w.num_q_heads,
             "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
             "window": w.window, "context": f"{kind}:{arg}", "mean_context": float(c.lengths[c.active == 1].mean()),
-            "kv_layout": kv_layout or kv_layout_desc(),
-            "l2": l2_note}
+            "kv_layout": kv_layout or kv_layout_desc()}
 
 
 # ------------------------------------------------------------------ CPU baseline (oracle)
@@ -373,14 +513,18 @@ def run_e2e(gk, shape, inputs, kv, out, ws, stream, dev, K, W, units, dist):
 
 
 # ------------------------------------------------------------------ main arms
-def run_gk(args):
+# Workloads reported beside the headline one, each measured in the same run.
+PER_CONFIG = ["tiny", "long_ctx", "ragged_b256", "swa_b512", "gk120b_rank_b64"]
+
+
+def measure_step(args, name, dev, dist, with_clocks=False, with_oracle=False):
+    """Time one workload: whole steps (append + attention, or the single-launch
+    step), the attention call alone (roofline), the append alone, and the
+    end-to-end loop from pinned host memory.  Returns the JSON fields."""
     import torch
     import paged_fp8_kv_gk_gb300 as gk
     rank, local_rank, world = dist_env()
-    torch.cuda.set_device(local_rank)
-    dist = dist_init("nccl")
-    dev = torch.device("cuda", local_rank)
-    w = gi.get(args.workload)
+    w = gi.get(name)
     c = gi.make_control(w)
     st = gi.make_step(w, dev)
     cache = gi.make_cache(w, c, dev)
@@ -459,7 +603,7 @@ def run_gk(args):
         one_step()
     torch.cuda.synchronize(dev)
     if gk.gk_read_device_error() != 0:
-        raise RuntimeError("device error word set during warm-up")
+        raise RuntimeError(f"{name}: device error word set during warm-up")
 
     # L2: a step whose KV is not well above the L2 size would find part of it
     # still cached from the step before; such steps are timed one by one with
@@ -485,12 +629,13 @@ def run_gk(args):
     # two ends so that nothing sits between the kernels of a step
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local_rank)
+    clocks = clock_sampler(dev) if with_clocks else None
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    clocks.start()
-    clocks.mark_begin()
+    if clocks:
+        clocks.start()
+        clocks.mark_begin()
     if flush:
         s0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
         s1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -505,8 +650,9 @@ def run_gk(args):
             one_step()
         ev1.record(stream)
     torch.cuda.synchronize(dev)
-    clocks.mark_end()
-    clk = clocks.stop()
+    if clocks:
+        clocks.mark_end()
+    clk = clocks.stop() if clocks else None
     if dist:
         dist.barrier()
     if flush:
@@ -538,7 +684,6 @@ def run_gk(args):
     units = gi.layer_seqs(w, c)
     max_ms, total_units = reduce_timing(elapsed_ms, units * K, dist, dev)
     value = total_units / (max_ms / 1e3)
-    ms_per_step = max_ms / K
 
     # ---- end to end: every step's inputs copied from pinned host memory (one
     # packed staging copy) and its output copied back, double-buffered on two
@@ -547,46 +692,75 @@ def run_gk(args):
     e2e_ms, e2e_units, h2d, d2h = run_e2e(gk, shape, dict(q=q, k_new=k_new, v_new=v_new, **ctl),
                                           kv, out, ws, stream, dev, K, W, units, dist)
     if gk.gk_read_device_error() != 0:
-        raise RuntimeError("device error word set during the timed region")
+        raise RuntimeError(f"{name}: device error word set during the timed region")
 
     # ---- roofline of the attention call
-    qo = gi.qo_bytes(w, c)
-    alg_bytes = kv_bytes + qo
+    ab = alg_bytes(w, c)
     peak, peak_kind = measured_peaks()
-    achieved = alg_bytes / (attn_ms / 1e3) / 1e9
-    traffic = recorded_traffic(w.name)
+    achieved = ab / (attn_ms / 1e3) / 1e9
+    tr = recorded_traffic(w, c)
+    res = {
+        "value": round(value, 1), "ms_per_step": round(max_ms / K, 4),
+        "config": workload_config(w, c, kv_layout_desc(args.k_layout, args.kv_form)),
+        "l2": l2_note,
+        "attn_ms": round(attn_ms, 4), "attn_ms_median": round(attn_med, 4),
+        "append_ms": round(append_ms, 4), "achieved_GBps": round(achieved, 1),
+        "kv_bytes_per_step": kv_bytes, "qo_bytes_per_step": gi.qo_bytes(w, c),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": tr[0] if tr else None,
+                     "traffic_source": (f"ncu dram__bytes_read.sum + dram__bytes_write.sum on "
+                                        f"{tr[1]}, scaled x{tr[2]:.4f} by algorithmic bytes"
+                                        if tr else None),
+                     "peak_source": peak_kind, "peak_nominal": NOMINAL_HBM_GBS,
+                     "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "kernel": "gk_decode_attn_stack (plan_kernel + attn_kernel)",
+                     "alg_bytes_per_launch": ab},
+        "e2e": {"value": round(e2e_units / (e2e_ms / 1e3), 1), "unit": UNIT,
+                "ms_per_step": round(e2e_ms / K, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "clocks": clk,
+    }
+    if with_oracle:
+        host = {k: gi.bf16_bits(v) for k, v in st.items()}
+        res["cpu_baseline"] = oracle_sample(w, c, host, cache, args.cpu_budget, k_layout=k_layout)
+    return res
+
+
+def run_gk(args):
+    import torch
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dist = dist_init("gloo")
+    dev = torch.device("cuda", local_rank)
+    K, W = args.steps, args.warmup
+    head = measure_step(args, args.workload, dev, dist, with_clocks=True,
+                        with_oracle=rank == 0 and world == 1 and not args.no_cpu_baseline)
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
-        "warmup": W, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "precision": "KV E4M3 codes; q/out bf16; QK^T and PV on f16 tensor-core MMA with fp32 "
                      "accumulation; fp32 online softmax",
         "data": "synthetic (seeded gk_inputs workload)",
-        "config": workload_config(w, c, l2_note, kv_layout_desc(args.k_layout, args.kv_form)),
         "impl": "gk",
-        "attn_ms": round(attn_ms, 4),
-        "attn_ms_median": round(attn_med, 4),
-        "append_ms": round(append_ms, 4),
-        "achieved_GBps": round(achieved, 1),
-        "kv_bytes_per_step": kv_bytes, "qo_bytes_per_step": qo,
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "peak_source": peak_kind,
-                     "peak_nominal": NOMINAL_HBM_GBS,
-                     "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
-                     "kernel": "gk_decode_attn_stack (plan_kernel + attn_kernel)",
-                     "alg_bytes_per_launch": alg_bytes},
-        "e2e": {"value": round(e2e_units / (e2e_ms / 1e3), 1), "unit": UNIT,
-                "ms_per_step": round(e2e_ms / K, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
         "step_form": args.step + (" (CUDA graph)" if args.graph else ""),
         "gpu_launches": (2 if args.step == "fused" else 3) * K,  # per timed step
-        "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        host = {k: gi.bf16_bits(v) for k, v in st.items()}
-        line["cpu_baseline"] = oracle_sample(w, c, host, cache, args.cpu_budget,
-                                             k_layout=k_layout)
+    line.update(head)
+    if world == 1 and not args.no_per_config and args.workload == DEFAULT_WORKLOAD:
+        per = {}
+        for name in PER_CONFIG:
+            r = measure_step(args, name, dev, dist)
+            per[name] = {"value": r["value"], "unit": UNIT, "ms_per_step": r["ms_per_step"],
+                         "attn_ms": r["attn_ms"], "achieved_GBps": r["achieved_GBps"],
+                         "frac": r["roofline"]["frac"],
+                         "frac_nominal": r["roofline"]["frac_nominal"],
+                         "traffic": r["roofline"]["traffic"], "e2e": r["e2e"]["value"],
+                         "alg_bytes_per_launch": r["roofline"]["alg_bytes_per_launch"],
+                         "config": r["config"], "l2": r["l2"]}
+            torch.cuda.empty_cache()
+        line["per_config"] = per
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -602,7 +776,7 @@ def run_ingest(args):
     import paged_fp8_kv_gk_gb300 as gk
     rank, local_rank, world = dist_env()
     torch.cuda.set_device(local_rank)
-    dist = dist_init("nccl")
+    dist = dist_init("gloo")
     dev = torch.device("cuda", local_rank)
     w = gi.get(args.workload)
     c = gi.make_control(w)
@@ -638,7 +812,7 @@ def run_ingest(args):
         return [e0[k].elapsed_time(e1[k]) for k in range(K)]
 
     K, W = args.steps, args.warmup
-    clocks = ClockSampler(local_rank)
+    clocks = clock_sampler(dev)
     clocks.start()
     clocks.mark_begin()
     per = timed(src, K, W)
@@ -657,9 +831,9 @@ def run_ingest(args):
         "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded gk_inputs workload)",
-        "config": dict(workload_config(w, c, f"inputs larger than L2: {landed / 1e9:.2f} GB landed "
-                                       "per step"), op="gk_kv_ingest", descriptors=int(dr.size),
+        "config": dict(workload_config(w, c), op="gk_kv_ingest", descriptors=int(dr.size),
                        block_len=int(src.shape[1])),
+        "l2": f"inputs larger than L2: {landed / 1e9:.2f} GB landed per step",
         "impl": "gk",
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peak_kind,
@@ -704,7 +878,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * wall / args.steps, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded gk_inputs workload)",
-        "config": workload_config(w, c, "host memory"), "impl": "reference",
+        "config": workload_config(w, c, kv_layout_desc(args.k_layout, args.kv_form)),
+        "l2": "host memory (the oracle runs on the host cores)", "impl": "reference",
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": T, "kind": "oracle",
                          "sample": f"each step one row x {w.num_layers} layers (all kv heads): "
                                    f"oracle append + fp64 attention; steps spread over {T} "
@@ -729,6 +904,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle CPU time for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure the headline workload only (no per_config block)")
     ap.add_argument("--step", choices=["split", "fused"], default="split",
                     help="split: gk_kv_append + gk_decode_attn_stack; fused: gk_decode_step")
     ap.add_argument("--k-layout", choices=["packed", "plain"], default="packed",
@@ -739,13 +916,17 @@ def main(argv=None):
                     help="time the step as one captured CUDA graph replayed per step")
     ap.add_argument("--record-traffic", metavar="LAUNCHES_CSV", default=None,
                     help="store the attention kernel's DRAM bytes per launch from an ncu launch "
-                         "list of --workload into profiles/attn_traffic.json, then exit")
+                         "list of the reduced case --workload (see traffic_command) into "
+                         "profiles/attn_traffic.json, then exit")
     ap.add_argument("--flush-l2", choices=["auto", "on", "off"], default="auto",
                     help="write twice the L2 size before every timed step (auto: when the KV "
                          "read per step is under twice the L2 size)")
     ap.add_argument("--ws-min", action="store_true",
                     help="use the minimum attention workspace (no split-KV chunks)")
     args = ap.parse_args(argv)
+    rc = launch_replicas(args.gpus, sys.argv[1:] if argv is None else list(argv))
+    if rc is not None:
+        sys.exit(rc)
     if args.record_traffic:
         print(json.dumps(record_traffic(args.workload or DEFAULT_WORKLOAD, args.record_traffic)))
         return

@@ -170,11 +170,25 @@ PROFILE = {
                                                      lengths="all:8192", seed=30),
     "gptoss_b8_8k": WORKLOADS["gptoss_b64"].replace(name="gptoss_b8_8k", batch=8,
                                                      lengths="all:8192", seed=31),
+    # reduced cases of the long-context and ragged workloads (a few GB of KV)
+    # for DRAM counters, scaled to the full workloads by algorithmic bytes
+    "long_b1": WORKLOADS["long_ctx"].replace(name="long_b1", batch=1, seed=35),
+    "ragged_b24": WORKLOADS["ragged_b256"].replace(name="ragged_b24", batch=24, seed=36),
+}
+
+# The page's deployed per-rank shape of the 120B GK decode (TP8: one kv head
+# per rank, 8 q heads, block 128, head 64) over the 36-layer stack, with the
+# batch and context mix of the batch-64 workload.
+RANK = {
+    "gk120b_rank_b64": WORKLOADS["gptoss_b64"].replace(
+        name="gk120b_rank_b64", num_q_heads=8, num_kv_heads=1, block_size=128, seed=37,
+        description="36 layers, batch 64, 8 q / 1 kv heads (one TP8 rank), block 128, "
+                    "L ~ U{1024..8192}"),
 }
 
 
 def get(name: str) -> Workload:
-    for table in (WORKLOADS, REDUCED, PROFILE, LANDING):
+    for table in (WORKLOADS, REDUCED, PROFILE, LANDING, RANK):
         if name in table:
             return table[name]
     raise KeyError(name)

@@ -46,3 +46,38 @@ def test_reduce_timing_two_ranks():
 def test_single_rank_needs_no_process_group():
     import bench
     assert bench.reduce_timing(3.0, 7.0, None) == (3.0, 7.0)
+
+
+def test_bench_gpus_flag_starts_its_own_ranks(tmp_path):
+    """bench.py --gpus 2 outside a launcher runs itself as two ranks
+    (torch.distributed.run on 127.0.0.1); the reference arm's rank 0 prints
+    the one JSON line, with n_gpus 2.  Under a launcher whose WORLD_SIZE is
+    not --gpus it refuses."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--impl",
+                        "reference", "--workload", "tiny", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, env=env, timeout=600, cwd=str(tmp_path))
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    assert lines[0]["n_gpus"] == 2 and lines[0]["impl"] == "reference"
+    env.update(WORLD_SIZE="3", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--impl",
+                        "reference", "--workload", "tiny"], capture_output=True, text=True,
+                       env=env, timeout=300, cwd=str(tmp_path))
+    assert r.returncode != 0 and "WORLD_SIZE=3" in r.stderr
+
+
+def test_reference_arm_config_matches_the_gpu_arm():
+    """Both arms describe the workload with the same config object."""
+    import bench
+    import gk_inputs as gi
+    w = gi.get("gptoss_b64")
+    c = gi.make_control(w)
+    assert bench.workload_config(w, c, bench.kv_layout_desc()) == bench.workload_config(w, c)

@@ -61,27 +61,51 @@ def test_appended_codes_helper_equals_whole_buffer_append(name):
             assert np.array_equal(vc[i, b], vview[pb, :, t, :])
 
 
-def test_bench_records_traffic_from_an_ncu_launch_list(tmp_path):
-    """bench.py --record-traffic: the attention kernel's launches are averaged
-    (other kernels ignored) and stamped with the current source hash."""
-    import bench
-    csv_path = tmp_path / "launches.csv"
+def _launch_list(path, launches):
     hdr = '"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",' \
           '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",' \
           '"Metric Value"\n'
     rows = []
-    for i, (k, rd, wr, t) in enumerate([("void attn_kernel<1, 0, 1>(AttnParams)", 100, 10, 5),
-                                        ("plan_kernel(PlanParams)", 7, 0, 1),
-                                        ("void attn_kernel<1, 0, 1>(AttnParams)", 300, 30, 7)]):
+    for i, (k, rd, wr, t) in enumerate(launches):
         for m, v in (("dram__bytes_read.sum", rd), ("dram__bytes_write.sum", wr),
                      ("gpu__time_duration.sum", t)):
             rows.append(f'"{i}","1","python","h","{k}","1","7","(128, 1, 1)","(608, 1, 1)","0",'
                         f'"10.3","Command line profiler metrics","{m}","byte","{v:,}"\n')
-    csv_path.write_text(hdr + "".join(rows))
+    path.write_text(hdr + "".join(rows))
+
+
+def test_bench_records_traffic_from_an_ncu_launch_list(tmp_path, monkeypatch):
+    """bench.py --record-traffic: the attention kernel's launches of a reduced
+    case are averaged (other kernels ignored), stamped with the current source
+    hash and the case's algorithmic bytes; the full workload's traffic is that
+    figure scaled by the ratio of algorithmic bytes."""
+    import json
+    import bench
+    csv_path = tmp_path / "launches.csv"
+    _launch_list(csv_path, [("void attn_kernel<1, 0, 1>(AttnParams)", 100, 10, 5),
+                            ("plan_kernel(PlanParams)", 7, 0, 1),
+                            ("void attn_kernel<1, 0, 1>(AttnParams)", 300, 30, 7)])
     out = tmp_path / "traffic.json"
-    e = bench.record_traffic("gptoss_b64", str(csv_path), str(out))
+    e = bench.record_traffic("gptoss_b16", str(csv_path), str(out))
     assert e["dram_read_bytes"] == 200 and e["dram_write_bytes"] == 20
     assert e["dram_bytes_per_launch"] == 220 and e["launches_averaged"] == 2
     assert e["kernel_src_sha"] == bench.attn_source_hash()
-    import json
-    assert json.loads(out.read_text())["gptoss_b64"]["dram_bytes_per_launch"] == 220
+    small = gi.get("gptoss_b16")
+    assert e["alg_bytes_per_launch"] == bench.alg_bytes(small, gi.make_control(small))
+    assert "-k regex:attn_kernel" in e["command"] and "-c 3" in e["command"]
+    assert json.loads(out.read_text())["gptoss_b16"]["dram_bytes_per_launch"] == 220
+    # the full workload reads its traffic from the reduced case, scaled
+    profiles = tmp_path / "profiles"
+    profiles.mkdir()
+    (profiles / "attn_traffic.json").write_text(out.read_text())
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "attn_source_hash", lambda: e["kernel_src_sha"])
+    full = gi.get("gptoss_b64")
+    cf = gi.make_control(full)
+    got, case, scale = bench.recorded_traffic(full, cf)
+    assert case == "gptoss_b16"
+    assert scale == pytest.approx(bench.alg_bytes(full, cf) / e["alg_bytes_per_launch"])
+    assert got == round(220 * scale)
+    # a capture taken on another kernel source is not used
+    monkeypatch.setattr(bench, "attn_source_hash", lambda: "0" * 16)
+    assert bench.recorded_traffic(full, cf) is None
