@@ -518,8 +518,8 @@ PER_CONFIG = ["tiny", "long_ctx", "ragged_b256", "swa_b512", "gk120b_rank_b64"]
 
 
 def measure_step(args, name, dev, dist, with_clocks=False, with_oracle=False):
-    """Time one workload: whole steps (append + attention, or the single-launch
-    step), the attention call alone (roofline), the append alone, and the
+    """Time one workload: whole steps (append + attention, or gk_decode_step),
+    the attention call alone (roofline), the append alone, and the
     end-to-end loop from pinned host memory.  Returns the JSON fields."""
     import torch
     import paged_fp8_kv_gk_gb300 as gk

@@ -204,19 +204,17 @@ gk_status gk_decode_attn_stack(const gk_shape *shape, const void *q, const gk_kv
                                void *workspace, size_t ws_bytes, void *stream);
 
 /*
- * gk_decode_step -- the whole decode step in one attention launch:
+ * gk_decode_step -- the whole decode step in two launches instead of three:
  * gk_kv_append followed by gk_decode_attn_stack, with the same arguments and
  * results (KV bytes identical to gk_kv_append's, outputs to
  * gk_decode_attn_stack's).  ("GPT-OSS-120B giga-kernel decode", section
  * "Kernel contract": one program consumes the new token's K/V, both update
  * indices and the attention-control tensors per step.)
- * The work unit that reads a row's new token (the last split-KV chunk of each
- * layer, row and kv head) computes that token's codes, stores them to the
- * cache and uses them in place of the bytes it staged; no other unit reads
- * those bytes.  This requires the control tensors to agree as the page builds
- * them: upd_full[b] is the slot of position pos[b] in row b of bt_full and
- * upd_swa[b] the slot of pos_w[b] in row b of bt_swa.  Inactive rows write
- * nothing and output zeros.  Errors: those of gk_kv_append and
+ * The append runs in CTAs beside the planner's, in the planner's launch; the
+ * attention launch starts while that grid runs and reads the plan and the
+ * cache only once the whole grid, append included, is complete.  The append
+ * starts once the work queued before the call is complete.  Inactive rows
+ * write nothing and output zeros.  Errors: those of gk_kv_append and
  * gk_decode_attn_stack.
  */
 gk_status gk_decode_step(const gk_shape *shape, const void *q, const void *k_new,

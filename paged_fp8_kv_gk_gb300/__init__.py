@@ -341,7 +341,7 @@ def gk_decode_attn_stack(shape, q, kv: KvCache, k_scale, v_scale, cos, sin, bt_f
 def gk_decode_step(shape, q, k_new, v_new, cos, sin, k_scale, v_scale, upd_full, upd_swa,
                    bt_full, bt_swa, pos, pos_w, active, kv: KvCache, out, out_f32=None,
                    workspace=None, stream=None, sinks=None) -> None:
-    """gk_kv_append + gk_decode_attn_stack in one attention launch."""
+    """gk_kv_append + gk_decode_attn_stack in two launches (the append in the planner's)."""
     import torch
     sh = _as_shape(shape)
     if workspace is None:

@@ -198,7 +198,7 @@ struct AppendInputs {
 };
 
 // Validation and launch shared by gk_decode_attn_stack and gk_decode_step
-// (app != nullptr: the fused step, where the units append the new token).
+// (app != nullptr: the single-launch step, whose planner grid also appends).
 static gk_status decode_attention(const gk_shape* shape, const void* q, const gk_kv_cache* kv,
                                   const float* k_scale, const float* v_scale,
                                   const float* cos, const float* sin, const int32_t* bt_full,
@@ -233,13 +233,6 @@ static gk_status decode_attention(const gk_shape* shape, const void* q, const gk
       p.kb[j] = kb[j];
       p.vb[j] = vb[j];
     }
-  }
-  if (app) {
-    p.fused = 1;
-    p.k_new = static_cast<const uint16_t*>(app->k_new);
-    p.v_new = static_cast<const uint16_t*>(app->v_new);
-    p.upd_full = app->upd_full;
-    p.upd_swa = app->upd_swa;
   }
   p.q = static_cast<const uint16_t*>(q);
   p.out = static_cast<uint16_t*>(out);
@@ -291,8 +284,34 @@ static gk_status decode_attention(const gk_shape* shape, const void* q, const gk
   pl.max_tokens_full = shape->max_blocks_full * shape->block_size;
   pl.max_tokens_swa = shape->max_blocks_swa * shape->block_size;
   pl.force_split_log = force_split_log;
-  return launch_attention(pl, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GK_OK
-                                                                                   : GK_ERR_CUDA;
+  AppendParams ap;
+  if (app) {
+    // the single-launch step: the append runs in the planner's grid
+    memset(&ap, 0, sizeof(ap));
+    ap.k_new = static_cast<const uint16_t*>(app->k_new);
+    ap.v_new = static_cast<const uint16_t*>(app->v_new);
+    ap.cosb = cos;
+    ap.sinb = sin;
+    ap.k_scale = k_scale;
+    ap.v_scale = v_scale;
+    ap.upd_full = app->upd_full;
+    ap.upd_swa = app->upd_swa;
+    ap.active = active;
+    for (int j = 0; j < shape->num_layers / 2; ++j) {
+      ap.kb[j] = const_cast<uint8_t*>(p.kb[j]);
+      ap.vb[j] = const_cast<uint8_t*>(p.vb[j]);
+    }
+    ap.k_packed = p.k_packed;
+    ap.NL = shape->num_layers;
+    ap.Bt = shape->batch;
+    ap.Hkv = shape->num_kv_heads;
+    ap.B = shape->block_size;
+    ap.nb = shape->num_blocks;
+  }
+  return launch_attention(pl, p, static_cast<cudaStream_t>(stream), app ? &ap : nullptr) ==
+                 cudaSuccess
+             ? GK_OK
+             : GK_ERR_CUDA;
 }
 
 }  // namespace gk

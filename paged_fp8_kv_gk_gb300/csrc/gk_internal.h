@@ -96,6 +96,12 @@ struct PlanParams {
   int force_split_log;
 };
 
+// The single-launch step's planner grid: CTA 0 plans, the others append.
+struct PlanAppendParams {
+  PlanParams plan;
+  AppendParams app;
+};
+
 struct AttnParams {
   const uint16_t* q;
   uint16_t* out;
@@ -117,12 +123,9 @@ struct AttnParams {
   int32_t* tickets;
   float* partials;
   int64_t cap;  // partial records per (layer pair, kv head) plane
-  // fused step (gk_decode_step): the unit holding the new token appends it first
-  const uint16_t* k_new;
-  const uint16_t* v_new;
-  const int32_t* upd_full;
-  const int32_t* upd_swa;
-  int fused;
+  // 36 bytes unused: they keep the offsets of the fields below, on which the
+  // attention kernel's measured speed depends
+  uint8_t reserved[36];
   int k_packed;  // 1: K through the packed view, 0: K laid out like V
   int NL, Bt, Hq, Hkv, B, nb, W, MBF, MBS;
   FastDiv fd_planes, fd_hkv, fd_nl, fd_b;  // (NL/2)*Hkv, Hkv, NL, B
@@ -144,7 +147,9 @@ struct IngestParams {
 // Launchers (gk_kernels.cu).  They return the launch status.
 cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
 cudaError_t launch_quantize(const float* x, float scale, uint8_t* codes, int64_t n, cudaStream_t st);
-cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaStream_t st);
+// app: the single-launch step's append, done in the planner's grid (or null).
+cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaStream_t st,
+                             const AppendParams* app = nullptr);
 // Resident warps of the persistent attention grid on the current device.
 int attention_resident_warps();
 cudaError_t read_device_error(cudaStream_t st, uint32_t* bits, bool clear);

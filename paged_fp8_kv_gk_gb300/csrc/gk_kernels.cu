@@ -3,7 +3,9 @@
 //   kv_append_kernel   RoPE(k) in IEEE fp32, / scale, E4M3 (RNE, satfinite),
 //                      scatter into the packed K and plain V layouts.
 //   plan_kernel        one CTA: split-KV chunk length, work-unit order
-//                      (largest first), per-row split bookkeeping.
+//                      (largest first), per-row split bookkeeping; in the
+//                      single-launch step, further CTAs of the same grid do
+//                      the KV append beside it.
 //   attn_kernel        persistent: each warp takes (layer, row, kv head, split)
 //                      units from an atomic counter, streams 32-token stages of
 //                      K and V through a private ring of 1-D bulk copies, and
@@ -48,16 +50,13 @@ __device__ __forceinline__ float div_scale(float x, float s, float r) {
 // One warp per (layer i, row b); kv heads in groups of 8.  Lane l rotates
 // the pair (l, l + 32) of k and converts channels 2l, 2l + 1 of v.  All of a
 // group's loads are issued before any of them is used (one memory round trip
-// per group rather than a chain of dependent ones).
+// per group rather than a chain of dependent ones).  P is AppendParams (the
+// append kernel) or AttnParams (the single-launch step, whose attention warps
+// append while the planner runs); ib = i * Bt + b.
 constexpr int kAppendHeads = 8;
 
-__global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ AppendParams p) {
-  // The decode-attention planner may launch now: it reads only positions and
-  // the active mask, and waits for this grid before it exits.
-  asm volatile("griddepcontrol.launch_dependents;");
-  const int lane = threadIdx.x & 31;
-  const int64_t ib = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (ib >= int64_t(p.NL) * p.Bt) return;
+template <class P>
+__device__ __forceinline__ void append_row(const P& p, int64_t ib, int lane) {
   const int b = int(ib % p.Bt);
   const int i = int(ib / p.Bt);
   const uint16_t* kr = p.k_new + ib * p.Hkv * kHeadDim;
@@ -91,12 +90,12 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ 
     // packed K: tokens 2p and 2p+1 interleaved per channel (channel e at byte
     // 2e of the pair row); plain K: laid out like V.  Either way a head's block
     // is B * D bytes.
-    uint8_t* kdst =
-        p.k_packed
-            ? p.kb[i >> 1] + ((pb * p.Hkv + h0) * (p.B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1)
-            : p.kb[i >> 1] + ((pb * p.Hkv + h0) * p.B + t) * kHeadDim;
+    uint8_t* kbase = const_cast<uint8_t*>(p.kb[i >> 1]);
+    uint8_t* kdst = p.k_packed
+                        ? kbase + ((pb * p.Hkv + h0) * (p.B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1)
+                        : kbase + ((pb * p.Hkv + h0) * p.B + t) * kHeadDim;
     const int estep = p.k_packed ? 2 : 1;
-    uint8_t* vdst = p.vb[i >> 1] + ((pb * p.Hkv + h0) * p.B + t) * kHeadDim;
+    uint8_t* vdst = const_cast<uint8_t*>(p.vb[i >> 1]) + ((pb * p.Hkv + h0) * p.B + t) * kHeadDim;
     const int64_t kstride = int64_t(p.B) * kHeadDim, vstride = int64_t(p.B) * kHeadDim;
 #pragma unroll
     for (int k = 0; k < kAppendHeads; ++k) {
@@ -116,6 +115,16 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ 
       }
     }
   }
+}
+
+__global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ AppendParams p) {
+  // The decode-attention planner may launch now: it reads only positions and
+  // the active mask, and waits for this grid before it exits.
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int lane = threadIdx.x & 31;
+  const int64_t ib = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (ib >= int64_t(p.NL) * p.Bt) return;
+  append_row(p, ib, lane);
 }
 
 __global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ x, float scale,
@@ -163,9 +172,8 @@ __device__ __forceinline__ long long warp_sum64(long long v) {
 // first; then one sliding-window entry per active row; then zero-fill units
 // (one per inactive row and layer).
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams p) {
-  // let the attention grid launch now; it waits for this grid before reading the plan
-  asm volatile("griddepcontrol.launch_dependents;");
+// The planner's work, done by one CTA.
+__device__ __forceinline__ void plan_body(const PlanParams& p) {
   extern __shared__ int32_t plan_sm[];
   int32_t* Ls = plan_sm;          // clamped context length per row (0 = no work)
   int32_t* Pw = plan_sm + p.Bt;   // window-frame position per row
@@ -488,6 +496,32 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams p) {
+  // let the attention grid launch now; it waits for this grid before reading the plan
+  asm volatile("griddepcontrol.launch_dependents;");
+  plan_body(p);
+}
+
+// Single-launch step: CTA 0 plans; the CTAs after it append the new token,
+// warp w taking (layer, row) pairs w, w + warps, ...  The attention grid waits
+// for this whole grid, so it reads the plan and the appended cache; the kernel
+// before this grid must be complete before the cache is written.
+__global__ void __launch_bounds__(kPlanThreads)
+    plan_append_kernel(const __grid_constant__ PlanAppendParams p) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (blockIdx.x == 0) {
+    plan_body(p.plan);
+    return;
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int64_t n_ib = int64_t(p.app.NL) * p.app.Bt;
+  const int64_t warps = (int64_t(gridDim.x) - 1) * (kPlanThreads / 32);
+  const int lane = threadIdx.x & 31;
+  for (int64_t ib = (int64_t(blockIdx.x) - 1) * (kPlanThreads / 32) + (threadIdx.x >> 5);
+       ib < n_ib; ib += warps)
+    append_row(p.app, ib, lane);
+}
+
 // =========================================================================
 // Decode attention (persistent)
 // =========================================================================
@@ -510,8 +544,6 @@ struct UnitDesc {
 constexpr uint32_t kQBytes = kGroup * kHeadDim * 2;
 constexpr uint32_t kRopeBytes = (kHeadDim / 2) * 4;
 constexpr uint32_t kUnitHeadBytes = kQBytes + 2 * kRopeBytes;
-// fused step: the new token's k and v rows (bf16) follow the unit head
-constexpr uint32_t kNewKvBytes = 2 * kHeadDim * 2;
 
 // The FMA comparison path keeps q' in fp32 (rows padded so the eight heads
 // fall in different banks) and one stage of P for the exchange between its
@@ -523,16 +555,14 @@ constexpr int kQfStride = kHeadDim + 4;
 template <bool kMma>
 struct alignas(128) WarpSmemT {
   uint8_t ring[kStages][kStageBytes];
-  uint8_t qbuf[kUnitHeadBytes + kNewKvBytes];
+  uint8_t qbuf[kUnitHeadBytes];
   float qf[kMma ? 4 : kGroup * kQfStride];
   float pbuf[kMma ? 4 : kStageTok * kGroup];
-  uint32_t apbuf[32];  // fused step: the new token's codes per lane
   unsigned long long bar[kStages];
   const uint8_t* pu_base[2];  // the producer unit's K and V bases (its kv head's bytes)
   // the producer unit's first stage is copied from key lo, its last stage up
   // to key hi of their 32-key stages (its range rounded out to 8): lo | hi << 8
   int pu_trim;
-  int32_t ap_slot[kFifo];  // fused step: update slot of each FIFO unit (copied asynchronously)
   int4 e_next;             // work descriptor of the claimed unit (copied asynchronously)
   UnitDesc fifo[kFifo];
 };
@@ -586,74 +616,14 @@ __device__ __forceinline__ void decode_unit(const AttnParams& p, int u, int4 e, 
   d.n_st = (e.z + kStageTok - 1) / kStageTok - d.st_begin;
 }
 
-// Fused step, kept out of line so that the stage loop's register allocation
-// is that of the plain kernel: (a) the new token's K and V codes from the rows
-// the unit's head copy brought, with gk_kv_append's arithmetic (lane l: k
-// channels l and l + 32 in the low half, v channels 2l, 2l + 1 in the high
-// half); (b) storing them at the update slot and into the staged copy.
-__device__ __noinline__ uint32_t fused_codes(const AttnParams& p, uint32_t qbuf0, int layer,
-                                             int lane) {
-  const uint32_t kr = qbuf0 + kUnitHeadBytes;
-  uint16_t kx16, ky16;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(kx16) : "r"(kr + 2 * lane));
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(ky16) : "r"(kr + 2 * (lane + 32)));
-  uint32_t vw, cb, sb;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(vw) : "r"(kr + kHeadDim * 2 + 4 * lane));
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(cb) : "r"(qbuf0 + kQBytes + 4 * lane));
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sb) : "r"(qbuf0 + kQBytes + kRopeBytes + 4 * lane));
-  const float x = __uint_as_float(uint32_t(kx16) << 16);
-  const float y = __uint_as_float(uint32_t(ky16) << 16);
-  const float c = __uint_as_float(cb), sn = __uint_as_float(sb);
-  const float ks = p.k_scale[layer], vs = p.v_scale[layer];
-  const float kr_inv = exact_reciprocal(ks), vr_inv = exact_reciprocal(vs);
-  const float xr = __fsub_rn(__fmul_rn(x, c), __fmul_rn(y, sn));
-  const float yr = __fadd_rn(__fmul_rn(y, c), __fmul_rn(x, sn));
-  return f32x2_to_e4m3x2(div_scale(xr, ks, kr_inv), div_scale(yr, ks, kr_inv)) |
-         (f32x2_to_e4m3x2(div_scale(bf16lo_to_f32(vw), vs, vr_inv),
-                          div_scale(bf16hi_to_f32(vw), vs, vr_inv))
-          << 16);
-}
-
-template <bool kPackedK>
-__device__ __noinline__ void fused_patch(const AttnParams& p, int32_t ap_slot, uint32_t ap_codes,
-                                         int layer, int kvh, int lane, uint32_t Ks, uint32_t Vs,
-                                         int tl) {
-  if (ap_slot < 0 || int64_t(ap_slot) >= int64_t(p.nb) * p.B) {
-    if (lane == 0) set_error(GK_DEVERR_SLOT);
-    return;
-  }
-  const int pbi = fdiv(ap_slot, p.fd_b);
-  const int64_t pb = pbi;
-  const int t = ap_slot - pbi * p.B;
-  constexpr int es = kPackedK ? 2 : 1;  // byte step between channels of a K row
-  uint8_t* kdst =
-      const_cast<uint8_t*>(p.kb[layer >> 1]) +
-      (kPackedK ? ((pb * p.Hkv + kvh) * (p.B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1)
-                : ((pb * p.Hkv + kvh) * p.B + t) * kHeadDim);
-  kdst[es * lane] = uint8_t(ap_codes & 0xffu);
-  kdst[es * (lane + 32)] = uint8_t((ap_codes >> 8) & 0xffu);
-  uint8_t* vdst = const_cast<uint8_t*>(p.vb[layer >> 1]) + ((pb * p.Hkv + kvh) * p.B + t) * kHeadDim;
-  reinterpret_cast<uint16_t*>(vdst)[lane] = uint16_t(ap_codes >> 16);
-  const uint32_t kp = kPackedK ? Ks + (tl >> 1) * (2 * kHeadDim) + (tl & 1) : Ks + tl * kHeadDim;
-  const uint16_t k0 = uint16_t(ap_codes & 0xffu), k1 = uint16_t((ap_codes >> 8) & 0xffu);
-  asm volatile("st.shared.u8 [%0], %1;" ::"r"(kp + es * lane), "h"(k0) : "memory");
-  asm volatile("st.shared.u8 [%0], %1;" ::"r"(kp + es * (lane + 32)), "h"(k1) : "memory");
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(Vs + tl * kHeadDim + 2 * lane),
-               "h"(uint16_t(ap_codes >> 16))
-               : "memory");
-}
-
 // kMma = true: QK^T and PV on the tensor cores (the product path).
 // kMma = false: the same pipeline with both products as fp32 FMA, kept to
 // measure the choice (selected with GK_ATTN_PATH=fma).
 // 4 CTAs (16 warps) per SM: latency hiding across warps measured worth more
 // than a deeper ring or the registers above 128.
-// kFused = true: the decode step's append is done by the units that read the
-// new token (gk_decode_step); a separate instantiation so that the plain
-// attention kernel keeps its own register allocation.
 // kPackedK: K through the packed view (tokens 2p, 2p+1 interleaved per
 // channel) or laid out like V.
-template <bool kMma, bool kFused, bool kPackedK>
+template <bool kMma, bool kPackedK>
 __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -725,17 +695,12 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   bool q_free = true;  // the q buffer may take the next unit's q
 
   // lane 0: copy the producer unit's q (8 heads) and its row's cos/sin rows
-  auto issue_unit_head = [&](uint32_t bar, bool appends, int layer, int b, int kvh) {
+  auto issue_unit_head = [&](uint32_t bar, int layer, int b, int kvh) {
     const uint16_t* qsrc =
         p.q + ((int64_t(layer) * p.Bt + b) * p.Hq + int64_t(kvh) * kGroup) * kHeadDim;
     bulk_g2s(qbuf0, qsrc, kQBytes, bar);
     bulk_g2s(qbuf0 + kQBytes, p.cosb + int64_t(b) * (kHeadDim / 2), kRopeBytes, bar);
     bulk_g2s(qbuf0 + kQBytes + kRopeBytes, p.sinb + int64_t(b) * (kHeadDim / 2), kRopeBytes, bar);
-    if (kFused && appends) {
-      const int64_t row = (int64_t(layer) * p.Bt + b) * p.Hkv + kvh;
-      bulk_g2s(qbuf0 + kUnitHeadBytes, p.k_new + row * kHeadDim, kHeadDim * 2, bar);
-      bulk_g2s(qbuf0 + kUnitHeadBytes + kHeadDim * 2, p.v_new + row * kHeadDim, kHeadDim * 2, bar);
-    }
   };
 
   // Next unit from the pipeline (warp-uniform); zero-fill units (inactive
@@ -774,7 +739,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
 
   auto issue_next = [&]() -> bool {
     if (exhausted) return false;
-    bool appends = false;  // fused step: the unit started here carries the new token
     int h_layer = 0, h_b = 0, h_kvh = 0;  // the unit started here (for its head copy)
     if (pk == pu_n_st) {
       if (!q_free) return false;  // the consumer has not read the buffered q yet
@@ -784,12 +748,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         return false;
       }
       if (lane == 0) ws.fifo[f_tail % kFifo] = d;
-      if constexpr (kFused) {
-        appends = d.s == d.ns - 1;
-        if (appends && lane == 0)
-          cp_async4(smem_u32(&ws.ap_slot[f_tail % kFifo]),
-                    d.kind == 2 ? p.upd_swa + d.b : p.upd_full + d.b);
-      }
       __syncwarp();
       ++f_tail;
       pk = 0;
@@ -815,7 +773,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       tn_ready = true;
     }
     const uint32_t head_bytes =
-        pk == 0 ? kUnitHeadBytes + ((kFused && appends) ? kNewKvBytes : 0u) : 0u;
+        pk == 0 ? kUnitHeadBytes : 0u;
     const uint32_t dst = ring0 + p_slot * kStageBytes;
     const uint32_t bar = bar0 + 8 * p_slot;
     const bool two = p.B < kStageTok;  // 16-token blocks: two per stage
@@ -849,7 +807,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       if (lane == 0) {
         const int64_t off = int64_t(pb0) * blk_bytes + pu_off * kHeadDim + lo_b;
         mbar_arrive_expect_tx(bar, 2 * kbytes + head_bytes);
-        if (head_bytes) issue_unit_head(bar, appends, h_layer, h_b, h_kvh);
+        if (head_bytes) issue_unit_head(bar, h_layer, h_b, h_kvh);
         bulk_g2s(dst + lo_b, ws.pu_base[0] + off, kbytes, bar);
         bulk_g2s(dst + kStageKBytes + lo_b, ws.pu_base[1] + off, kbytes, bar);
       }
@@ -870,7 +828,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       if (lane == 0) {
         const uint32_t half = uint32_t(p.B) * kHeadDim;
         mbar_arrive_expect_tx(bar, (has1 ? 4 * half : 2 * half) + head_bytes);
-        if (head_bytes) issue_unit_head(bar, appends, h_layer, h_b, h_kvh);
+        if (head_bytes) issue_unit_head(bar, h_layer, h_b, h_kvh);
         const int64_t o0 = int64_t(pb0) * blk_bytes;
         bulk_g2s(dst, ws.pu_base[0] + o0, half, bar);
         bulk_g2s(dst + kStageKBytes, ws.pu_base[1] + o0, half, bar);
@@ -911,8 +869,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   // FMA path: per-head reference maxima / thresholds (log2 units, warp-uniform)
   // and this lane's partial denominators (lane = token)
   float mh[kMma ? 1 : kGroup], thh[kMma ? 1 : kGroup], lsum[kMma ? 1 : kGroup];
-  // fused step: codes of the new token (lane l: k channels l, l+32; v channels
-  // 2l, 2l+1) and its update slot, computed at the unit's start
 
   while (prod - cons < kStages && issue_next()) {
   }
@@ -932,10 +888,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
       cd.t_end = CU.t_end;
       cd.st_begin = CU.st_begin;
       cd.n_st = CU.n_st;
-      if constexpr (kFused) {
-        // the new token's codes, kept to the unit's last stage
-        if (CU.s == CU.ns - 1) ws.apbuf[lane] = fused_codes(p, qbuf0, CU.layer, lane);
-      }
       // ---- unit prologue: rotated q for head (kvh*8 + g), channels 16qd..16qd+15
       const uint32_t qrow = qbuf0 + g * (kHeadDim * 2);
       const uint4 x0 = lds128(qrow + 32 * qd);
@@ -1017,18 +969,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
     const uint32_t Vs = Ks + kStageKBytes;
     const int tok0 = (cd.st_begin + k_in_unit) * kStageTok;
     const bool edge = tok0 < cd.t_begin || tok0 + kStageTok > cd.t_end;
-    if constexpr (kFused) {
-      if (k_in_unit == cd.n_st - 1 && CU.s == CU.ns - 1) {
-        // the new token is the last key of the unit: store its codes to the
-        // cache and into the staged copy (which holds the bytes from before)
-        if (lane == 0) cp_async_wait_all();
-        __syncwarp();
-        fused_patch<kPackedK>(p, ws.ap_slot[f_head % kFifo], ws.apbuf[lane], CU.layer, CU.kvh,
-                              lane, Ks, Vs, cd.t_end - 1 - tok0);
-        __syncwarp();
-      }
-    }
-
     if constexpr (kMma) {
     // ---- S = q' K^T for two 16-token tiles; rows (g, g+8) = tokens (2g+sw, 2g+1-sw)
     // of the tile, sw = 0 for packed K; for plain K sw = g & 1, so that lanes of
@@ -1451,12 +1391,10 @@ struct DeviceCache {
 };
 static DeviceCache g_cache[64];
 
-// Attention instantiations, index = fma * 4 + fused * 2 + plain_k.
-static const void* const kAttnKernels[8] = {
-    (const void*)attn_kernel<true, false, true>,   (const void*)attn_kernel<true, false, false>,
-    (const void*)attn_kernel<true, true, true>,    (const void*)attn_kernel<true, true, false>,
-    (const void*)attn_kernel<false, false, true>,  (const void*)attn_kernel<false, false, false>,
-    (const void*)attn_kernel<false, true, true>,   (const void*)attn_kernel<false, true, false>};
+// Attention instantiations, index = fma * 2 + plain_k.
+static const void* const kAttnKernels[4] = {
+    (const void*)attn_kernel<true, true>, (const void*)attn_kernel<true, false>,
+    (const void*)attn_kernel<false, true>, (const void*)attn_kernel<false, false>};
 
 static cudaError_t device_setup(DeviceCache** out) {
   int dev = 0;
@@ -1472,8 +1410,8 @@ static cudaError_t device_setup(DeviceCache** out) {
     // every instantiation of the selected path is launched with the smallest
     // occupancy among them, so that all fit the same persistent grid
     c.attn_blocks_per_sm = 1 << 30;
-    for (int k = 0; k < 8; ++k) {
-      const bool mma = (k & 4) == 0;
+    for (int k = 0; k < 4; ++k) {
+      const bool mma = (k & 2) == 0;
       const size_t smem = mma ? attn_smem<true>() : attn_smem<false>();
       e = cudaFuncSetAttribute(kAttnKernels[k], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                int(smem));
@@ -1486,6 +1424,9 @@ static cudaError_t device_setup(DeviceCache** out) {
       if (blocks < c.attn_blocks_per_sm) c.attn_blocks_per_sm = blocks;
     }
     e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(2 * kMaxBatch * sizeof(int32_t)));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(plan_append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(2 * kMaxBatch * sizeof(int32_t)));
     if (e != cudaSuccess) return e;
     if (c.attn_blocks_per_sm < 1) c.attn_blocks_per_sm = 1;
@@ -1524,7 +1465,8 @@ cudaError_t launch_quantize(const float* x, float scale, uint8_t* codes, int64_t
   return cudaGetLastError();
 }
 
-cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaStream_t st) {
+cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaStream_t st,
+                             const AppendParams* app) {
   DeviceCache* c = nullptr;
   cudaError_t e = device_setup(&c);
   if (e != cudaSuccess) return e;
@@ -1544,7 +1486,18 @@ cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaSt
   pcfg.stream = st;
   pcfg.attrs = attr;
   pcfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&pcfg, plan_kernel, pp);
+  if (app) {
+    // the single-launch step appends in CTAs beside the planner's: one warp
+    // per (layer, row) pair
+    PlanAppendParams pa;
+    pa.plan = pp;
+    pa.app = *app;
+    pcfg.gridDim = dim3(unsigned(1 + (int64_t(app->NL) * app->Bt * 32 + kPlanThreads - 1) /
+                                         kPlanThreads));
+    e = cudaLaunchKernelEx(&pcfg, plan_append_kernel, pa);
+  } else {
+    e = cudaLaunchKernelEx(&pcfg, plan_kernel, pp);
+  }
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(c->sms * c->attn_blocks_per_sm));
@@ -1553,7 +1506,7 @@ cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaSt
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const int k = (c->fma ? 4 : 0) + (p.fused ? 2 : 0) + (p.k_packed ? 0 : 1);
+  const int k = (c->fma ? 2 : 0) + (p.k_packed ? 0 : 1);
   void* args[] = {const_cast<AttnParams*>(&p)};
   return cudaLaunchKernelExC(&cfg, kAttnKernels[k], args);
 }

@@ -2,7 +2,7 @@
  * decode_step.c -- one decode step through the C ABI alone (include/gk.h), no
  * Python: the program reads a step's inputs from raw little-endian files in a
  * directory, uploads them, runs gk_kv_append and gk_decode_attn_stack (or the
- * single-launch gk_decode_step) on CUDA device 0, checks the device error word
+ * gk_decode_step) on CUDA device 0, checks the device error word
  * and writes the output and the group buffers back.
  *
  *   usage: decode_step <dir> [split|fused]

@@ -1,7 +1,7 @@
 """The C ABI used from C alone: paged_fp8_kv_gk_gb300/examples/decode_step.c
 (built here with the system C compiler against libgk.so and the CUDA runtime)
 runs one decode step from raw input files, as append + attention or as the
-single-launch step, with or without attention sinks; its output and group
+two-launch step (gk_decode_step), with or without attention sinks; its output and group
 buffers match the oracle (bf16 output within the parity tolerance, KV bytes
 bit-exact)."""
 import os

@@ -109,8 +109,8 @@ def test_last_wave_pieces(step):
     wave, so the planner cuts chunks of those rows into pieces that run at the
     end (header word 7 counts them).  Pieces change only where the splits
     fall: every appended KV byte stays bit-exact and sampled outputs meet the
-    tolerance, in the two-launch and the single-launch step (whose last piece
-    or remainder of each row appends the token)."""
+    tolerance, with gk_kv_append + gk_decode_attn_stack and with
+    gk_decode_step."""
     w = gi.get("long_cut_small")
     c = gi.make_control(w)
     st = gi.make_step(w, "cuda")

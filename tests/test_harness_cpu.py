@@ -82,9 +82,9 @@ def test_bench_records_traffic_from_an_ncu_launch_list(tmp_path, monkeypatch):
     import json
     import bench
     csv_path = tmp_path / "launches.csv"
-    _launch_list(csv_path, [("void attn_kernel<1, 0, 1>(AttnParams)", 100, 10, 5),
+    _launch_list(csv_path, [("void attn_kernel<1, 1>(AttnParams)", 100, 10, 5),
                             ("plan_kernel(PlanParams)", 7, 0, 1),
-                            ("void attn_kernel<1, 0, 1>(AttnParams)", 300, 30, 7)])
+                            ("void attn_kernel<1, 1>(AttnParams)", 300, 30, 7)])
     out = tmp_path / "traffic.json"
     e = bench.record_traffic("gptoss_b16", str(csv_path), str(out))
     assert e["dram_read_bytes"] == 200 and e["dram_write_bytes"] == 20
