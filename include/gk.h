@@ -238,8 +238,9 @@ gk_status gk_decode_step(const gk_shape *shape, const void *q, const void *k_new
  * the workspace.  Arguments and results are those of gk_decode_attn_stack
  * (the caller still passes inputs and outputs).
  *   - Returns GK_ERR_WORKSPACE when the shape needs more than
- *     GK_STATIC_SCRATCH_BYTES of workspace (gk_attn_workspace_min_bytes); a
- *     smaller array than the recommended workspace only means fewer split-KV
+ *     GK_STATIC_SCRATCH_BYTES of workspace (gk_attn_workspace_min_bytes); no
+ *     shape the library accepts does (the largest needs under 1 MiB).  An
+ *     array smaller than the recommended workspace only means fewer split-KV
  *     chunks.
  *   - Every call looks up the array's device address in the current context
  *     (cudaGetSymbolAddress, with the caller's device current; no work is

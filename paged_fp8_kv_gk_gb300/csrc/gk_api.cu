@@ -96,8 +96,8 @@ WsLayout ws_layout(const gk_shape& s, size_t ws_bytes) {
     o = align256(o + size_t(s.batch) * sizeof(int32_t));
     L.part_base = o;
     o = align256(o + size_t(s.batch) * sizeof(int32_t));
-    L.tickets = o;
-    o = align256(o + size_t(planes) * s.batch * sizeof(int32_t));
+    L.split_rows = o;
+    o = align256(o + size_t(s.batch) * sizeof(int32_t));
     L.partials = o;
     o = align256(o + size_t(cap) * size_t(planes) * rec);
     L.total = o;
@@ -249,7 +249,7 @@ static gk_status decode_attention(const gk_shape* shape, const void* q, const gk
   p.edesc = reinterpret_cast<const int4*>(ws + L.edesc);
   p.zero_list = reinterpret_cast<const int32_t*>(ws + L.zero_list);
   p.part_base = reinterpret_cast<const int32_t*>(ws + L.part_base);
-  p.tickets = reinterpret_cast<int32_t*>(ws + L.tickets);
+  p.split_rows = reinterpret_cast<const int32_t*>(ws + L.split_rows);
   p.partials = reinterpret_cast<float*>(ws + L.partials);
   p.cap = L.cap;
   p.NL = shape->num_layers;
@@ -275,7 +275,7 @@ static gk_status decode_attention(const gk_shape* shape, const void* q, const gk
   pl.edesc = reinterpret_cast<int4*>(ws + L.edesc);
   pl.zero_list = reinterpret_cast<int32_t*>(ws + L.zero_list);
   pl.part_base = reinterpret_cast<int32_t*>(ws + L.part_base);
-  pl.tickets = reinterpret_cast<int32_t*>(ws + L.tickets);
+  pl.split_rows = reinterpret_cast<int32_t*>(ws + L.split_rows);
   pl.cap = L.cap;
   pl.NL = shape->num_layers;
   pl.Bt = shape->batch;

@@ -223,6 +223,12 @@ __device__ __forceinline__ float4 ldg_cg_f4(const float* p) {
   return v;
 }
 
+__device__ __forceinline__ float2 ldg_cg_f2(const float* p) {
+  float2 v;
+  asm volatile("ld.global.cg.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ float ldg_cg_f(const float* p) {
   float v;
   asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));

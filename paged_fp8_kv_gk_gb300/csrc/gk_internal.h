@@ -50,11 +50,12 @@ enum HdrWord {
   kHdrNEntries = 5,
   kHdrTotalSplits = 6,
   kHdrPieces = 7,       // pieces cut from chunks of long rows for the last wave (0: none)
+  kHdrSplitRows = 9,    // rows with split-KV partials (entries of the split-row list)
   kHdrWords = 64
 };
 
 struct WsLayout {
-  size_t hdr, edesc, zero_list, part_base, tickets, partials, total;
+  size_t hdr, edesc, zero_list, part_base, split_rows, partials, total;
   int64_t cap;          // partial records per (layer pair, kv head) plane
   int64_t max_entries;
 };
@@ -86,7 +87,7 @@ struct PlanParams {
   int4* edesc;
   int32_t* zero_list;
   int32_t* part_base;
-  int32_t* tickets;
+  int32_t* split_rows;  // rows with split-KV partials: b | ns << 16
   int64_t cap;
   int NL, Bt, Hkv, W, n_warps;
   int max_tokens_full, max_tokens_swa;  // table row lengths in tokens
@@ -120,7 +121,7 @@ struct AttnParams {
   const int4* edesc;
   const int32_t* zero_list;
   const int32_t* part_base;
-  int32_t* tickets;
+  const int32_t* split_rows;
   float* partials;
   int64_t cap;  // partial records per (layer pair, kv head) plane
   // 36 bytes unused: they keep the offsets of the fields below, on which the

@@ -11,8 +11,9 @@
 //                      K and V through a private ring of 1-D bulk copies, and
 //                      runs QK^T and PV on the tensor cores (mma.sync m16n8k16,
 //                      N = the 8 q heads of the GQA group) with an online
-//                      softmax.  Split units write (m, l, o) partials; the last
-//                      of a row's splits to finish merges them.
+//                      softmax.  Split units write (m, l, o) partials.
+//   combine_kernel     the split-KV (flash-decoding) combine: one warp per
+//                      (row with partials, layer pair, kv head) merges them.
 //
 // Page references: "GPT-OSS-120B giga-kernel decode", sections "Kernel
 // contract" (layer parity i % 2 selects table / index / position, buffer
@@ -185,6 +186,7 @@ __device__ __forceinline__ void plan_body(const PlanParams& p) {
   __shared__ long long s_red[3][kPlanWarps];
   __shared__ int s_bucket[kRemBuckets];
   __shared__ int4 s_scan[kPlanWarps];
+  __shared__ int s_nsr[kPlanWarps];
   __shared__ int s_S_log;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int chunk = (p.Bt + kPlanThreads - 1) / kPlanThreads;
@@ -362,6 +364,7 @@ __device__ __forceinline__ void plan_body(const PlanParams& p) {
     return min(c, nf);
   };
   int4 cnt = make_int4(0, 0, 0, 0);
+  int nsr = 0;  // rows with split-KV partials
   int rk = erank;
   for (int b = b_lo; b < b_hi; ++b) {
     const int L = Ls[b];
@@ -370,6 +373,7 @@ __device__ __forceinline__ void plan_body(const PlanParams& p) {
       const int ns = nf + cut * (conv_p - 1) + (r > 0);
       cnt.x += nf - cut;
       cnt.y += ns > 1 ? ns : 0;
+      nsr += ns > 1;
       cnt.z += 1;
       if (r > 0) {
         cnt.w += 1;
@@ -393,8 +397,22 @@ __device__ __forceinline__ void plan_body(const PlanParams& p) {
       inc.w += w;
     }
   }
-  if (lane == 31) s_scan[wid] = inc;
+  int nsr_inc = nsr;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, nsr_inc, o);
+    if (lane >= o) nsr_inc += y;
+  }
+  if (lane == 31) {
+    s_scan[wid] = inc;
+    s_nsr[wid] = nsr_inc;
+  }
   __syncthreads();
+  int srp = nsr_inc - nsr, n_split_rows = 0;  // this thread's first slot in the split-row list
+  for (int w = 0; w < kPlanWarps; ++w) {
+    if (w < wid) srp += s_nsr[w];
+    n_split_rows += s_nsr[w];
+  }
   int4 base = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
   for (int w = 0; w < kPlanWarps; ++w) {
     const int4 v = s_scan[w];
@@ -463,8 +481,7 @@ __device__ __forceinline__ void plan_body(const PlanParams& p) {
       if (ns > 1) {
         p.part_base[b] = sp;
         sp += ns;
-        for (int j = 0; j < (p.NL >> 1); ++j)
-          for (int h = 0; h < p.Hkv; ++h) p.tickets[(int64_t(j) * p.Bt + b) * p.Hkv + h] = 0;
+        p.split_rows[srp++] = b | (ns << 16);
       } else {
         p.part_base[b] = 0;
       }
@@ -489,6 +506,7 @@ __device__ __forceinline__ void plan_body(const PlanParams& p) {
     p.hdr[kHdrNEntries] = NEF + NA;
     p.hdr[kHdrTotalSplits] = TS;
     p.hdr[kHdrPieces] = conv_p > 0 ? (conv_c * s_ne[s_S_log] + conv_x) * conv_p : 0;
+    p.hdr[kHdrSplitRows] = n_split_rows;
   }
   // This grid may have started while the kernel before it (the KV append)
   // was still running; it completes only after that kernel has, so the
@@ -642,6 +660,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
 
   // the planner grid (launched just before) must be complete from here on
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the combine grid may launch now; it waits for this grid before reading
+  asm volatile("griddepcontrol.launch_dependents;");
   const int nU = p.hdr[kHdrNUnits];
   const int nAll = nU + p.hdr[kHdrNZero];  // units with a descriptor, then zero-fill units
 
@@ -1256,7 +1276,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
           f1[1] = make_float4(r1[4], r1[5], r1[6], r1[7]);
         }
       } else {
-        // split partial: (m, l, o) unnormalised, in log2 units
+        // split partial: (m, l, o) unnormalised, in log2 units, for the combine kernel
         const int j = CU.layer >> 1;
         const int64_t plane = int64_t(j) * p.Hkv + CU.kvh;
         const int64_t cap = p.cap;
@@ -1273,74 +1293,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
         ro0[1] = make_float4(o[2][0], o[2][2], o[3][0], o[3][2]);
         ro1[0] = make_float4(o[0][1], o[0][3], o[1][1], o[1][3]);
         ro1[1] = make_float4(o[2][1], o[2][3], o[3][1], o[3][3]);
-        // the warp barrier orders every lane's partial stores before lane 0's
-        // release; the last arriver's acquire (then the barrier) orders its
-        // reads of the other splits' partials after their releases
-        __syncwarp();
-        int old = 0;
-        int32_t* ticket = p.tickets + (int64_t(j) * p.Bt + CU.b) * p.Hkv + CU.kvh;
-        if (lane == 0) old = atom_add_acq_rel_gpu(ticket, 1);
-        old = __shfl_sync(kFull, old, 0);
-        if (old == CU.ns - 1) {
-          // last split to finish: merge all of this row's partials in split order
-          __syncwarp();
-          const float* base = p.partials + (plane * cap + p.part_base[CU.b]) * kPartialFloats;
-          float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
-          float a0[8], a1[8];
-#pragma unroll
-          for (int c = 0; c < 8; ++c) a0[c] = a1[c] = 0.f;
-          for (int s = 0; s < CU.ns; ++s) {
-            const float* rs = base + int64_t(s) * kPartialFloats;
-            const float ms0 = ldg_cg_f(rs + 2 * qd), ms1 = ldg_cg_f(rs + 2 * qd + 1);
-            const float ls0 = ldg_cg_f(rs + kGroup + 2 * qd), ls1 = ldg_cg_f(rs + kGroup + 2 * qd + 1);
-            const float* os0 = rs + 2 * kGroup + (2 * qd) * kHeadDim + 8 * g;
-            const float* os1 = rs + 2 * kGroup + (2 * qd + 1) * kHeadDim + 8 * g;
-            const float4 p00 = ldg_cg_f4(os0), p01 = ldg_cg_f4(os0 + 4);
-            const float4 p10 = ldg_cg_f4(os1), p11 = ldg_cg_f4(os1 + 4);
-            const float n0 = fmaxf(M0, ms0), n1 = fmaxf(M1, ms1);
-            const float c0 = ex2(M0 - n0), w0 = ex2(ms0 - n0);
-            const float c1 = ex2(M1 - n1), w1 = ex2(ms1 - n1);
-            M0 = n0;
-            M1 = n1;
-            L0 = L0 * c0 + ls0 * w0;
-            L1 = L1 * c1 + ls1 * w1;
-            const float q0[8] = {p00.x, p00.y, p00.z, p00.w, p01.x, p01.y, p01.z, p01.w};
-            const float q1[8] = {p10.x, p10.y, p10.z, p10.w, p11.x, p11.y, p11.z, p11.w};
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              a0[c] = a0[c] * c0 + q0[c] * w0;
-              a1[c] = a1[c] * c1 + q1[c] * w1;
-            }
-          }
-          const float* snk =
-              p.sinks ? p.sinks + int64_t(CU.layer) * p.Hq + CU.kvh * kGroup + 2 * qd : nullptr;
-          const float i0 = out_scale(L0, M0, snk, vscale);
-          const float i1 = out_scale(L1, M1, snk ? snk + 1 : nullptr, vscale);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            a0[c] *= i0;
-            a1[c] *= i1;
-          }
-          uint4 u0, u1;
-          u0.x = f32x2_to_bf16x2(a0[0], a0[1]);
-          u0.y = f32x2_to_bf16x2(a0[2], a0[3]);
-          u0.z = f32x2_to_bf16x2(a0[4], a0[5]);
-          u0.w = f32x2_to_bf16x2(a0[6], a0[7]);
-          u1.x = f32x2_to_bf16x2(a1[0], a1[1]);
-          u1.y = f32x2_to_bf16x2(a1[2], a1[3]);
-          u1.z = f32x2_to_bf16x2(a1[4], a1[5]);
-          u1.w = f32x2_to_bf16x2(a1[6], a1[7]);
-          *reinterpret_cast<uint4*>(p.out + out_row) = u0;
-          *reinterpret_cast<uint4*>(p.out + out_row + kHeadDim) = u1;
-          if (p.out_f32) {
-            float4* f0 = reinterpret_cast<float4*>(p.out_f32 + out_row);
-            float4* f1 = reinterpret_cast<float4*>(p.out_f32 + out_row + kHeadDim);
-            f0[0] = make_float4(a0[0], a0[1], a0[2], a0[3]);
-            f0[1] = make_float4(a0[4], a0[5], a0[6], a0[7]);
-            f1[0] = make_float4(a1[0], a1[1], a1[2], a1[3]);
-            f1[1] = make_float4(a1[4], a1[5], a1[6], a1[7]);
-          }
-        }
       }
       ++f_head;
     }
@@ -1359,6 +1311,114 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   }
 }
 
+
+// =========================================================================
+// Split-KV combine (flash-decoding)
+// =========================================================================
+// One warp per (split row, plane = (layer pair j, kv head)) merges the ns
+// partial records of full layer 2j + 1, row b, kv head into the output.  Lane
+// (g, qd) produces heads 2qd, 2qd + 1, channels 8g .. 8g + 7.  The partials
+// are read kCombineAhead at a time (their loads in flight together) and
+// folded in split order -- the same order whatever order the splits finished
+// in -- with a running maximum; then the output scale (attention sink
+// included) and the bf16 (+ fp32) stores.
+constexpr int kCombineThreads = 128;
+constexpr int kCombineBlocksPerSm = 4;
+constexpr int kCombineAhead = 4;
+
+__global__ void __launch_bounds__(kCombineThreads, kCombineBlocksPerSm)
+    combine_kernel(const __grid_constant__ AttnParams p) {
+  // the attention grid (launched just before) must be complete: its partials
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31, g = lane >> 2, qd = lane & 3;
+  const int n_rows = p.hdr[kHdrSplitRows];
+  const int planes = int(p.fd_planes.d);
+  const int n_items = n_rows * planes;  // <= 8192 rows x 4096 planes
+  const int warps = int(gridDim.x) * (kCombineThreads / 32);
+  for (int it = int(blockIdx.x) * (kCombineThreads / 32) + (threadIdx.x >> 5); it < n_items;
+       it += warps) {
+    const int r = fdiv(it, p.fd_planes);
+    const int plane = it - r * planes;
+    const int e = p.split_rows[r];
+    const int b = e & 0xffff, ns = e >> 16;
+    const int j = fdiv(plane, p.fd_hkv);
+    const int kvh = plane - j * p.Hkv;
+    const int layer = 2 * j + 1;
+    const float* base = p.partials + (int64_t(plane) * p.cap + p.part_base[b]) * kPartialFloats;
+    float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
+    float a0[8], a1[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) a0[c] = a1[c] = 0.f;
+    for (int s0 = 0; s0 < ns; s0 += kCombineAhead) {
+      float2 ms[kCombineAhead], ls[kCombineAhead];
+      float4 o00[kCombineAhead], o01[kCombineAhead], o10[kCombineAhead], o11[kCombineAhead];
+#pragma unroll
+      for (int k = 0; k < kCombineAhead; ++k) {
+        if (s0 + k < ns) {
+          const float* rs = base + int64_t(s0 + k) * kPartialFloats;
+          ms[k] = ldg_cg_f2(rs + 2 * qd);
+          ls[k] = ldg_cg_f2(rs + kGroup + 2 * qd);
+          const float* os0 = rs + 2 * kGroup + (2 * qd) * kHeadDim + 8 * g;
+          o00[k] = ldg_cg_f4(os0);
+          o01[k] = ldg_cg_f4(os0 + 4);
+          o10[k] = ldg_cg_f4(os0 + kHeadDim);
+          o11[k] = ldg_cg_f4(os0 + kHeadDim + 4);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kCombineAhead; ++k) {
+        if (s0 + k < ns) {
+          const float n0 = fmaxf(M0, ms[k].x), n1 = fmaxf(M1, ms[k].y);
+          const float c0 = ex2(M0 - n0), w0 = ex2(ms[k].x - n0);
+          const float c1 = ex2(M1 - n1), w1 = ex2(ms[k].y - n1);
+          M0 = n0;
+          M1 = n1;
+          L0 = fmaf(L0, c0, ls[k].x * w0);
+          L1 = fmaf(L1, c1, ls[k].y * w1);
+          const float q0[8] = {o00[k].x, o00[k].y, o00[k].z, o00[k].w,
+                               o01[k].x, o01[k].y, o01[k].z, o01[k].w};
+          const float q1[8] = {o10[k].x, o10[k].y, o10[k].z, o10[k].w,
+                               o11[k].x, o11[k].y, o11[k].z, o11[k].w};
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            a0[c] = fmaf(a0[c], c0, q0[c] * w0);
+            a1[c] = fmaf(a1[c], c1, q1[c] * w1);
+          }
+        }
+      }
+    }
+    const float* snk = p.sinks ? p.sinks + int64_t(layer) * p.Hq + kvh * kGroup + 2 * qd : nullptr;
+    const float vscale = p.v_scale[layer];
+    const float i0 = out_scale(L0, M0, snk, vscale);
+    const float i1 = out_scale(L1, M1, snk ? snk + 1 : nullptr, vscale);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      a0[c] *= i0;
+      a1[c] *= i1;
+    }
+    const int64_t out_row =
+        ((int64_t(layer) * p.Bt + b) * p.Hq + kvh * kGroup + 2 * qd) * kHeadDim + 8 * g;
+    uint4 u0, u1;
+    u0.x = f32x2_to_bf16x2(a0[0], a0[1]);
+    u0.y = f32x2_to_bf16x2(a0[2], a0[3]);
+    u0.z = f32x2_to_bf16x2(a0[4], a0[5]);
+    u0.w = f32x2_to_bf16x2(a0[6], a0[7]);
+    u1.x = f32x2_to_bf16x2(a1[0], a1[1]);
+    u1.y = f32x2_to_bf16x2(a1[2], a1[3]);
+    u1.z = f32x2_to_bf16x2(a1[4], a1[5]);
+    u1.w = f32x2_to_bf16x2(a1[6], a1[7]);
+    *reinterpret_cast<uint4*>(p.out + out_row) = u0;
+    *reinterpret_cast<uint4*>(p.out + out_row + kHeadDim) = u1;
+    if (p.out_f32) {
+      float4* f0 = reinterpret_cast<float4*>(p.out_f32 + out_row);
+      float4* f1 = reinterpret_cast<float4*>(p.out_f32 + out_row + kHeadDim);
+      f0[0] = make_float4(a0[0], a0[1], a0[2], a0[3]);
+      f0[1] = make_float4(a0[4], a0[5], a0[6], a0[7]);
+      f1[0] = make_float4(a1[0], a1[1], a1[2], a1[3]);
+      f1[1] = make_float4(a1[4], a1[5], a1[6], a1[7]);
+    }
+  }
+}
 
 // =========================================================================
 // Test hook: the bounded barrier wait running out
@@ -1508,7 +1568,15 @@ cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaSt
   cfg.numAttrs = 1;
   const int k = (c->fma ? 2 : 0) + (p.k_packed ? 0 : 1);
   void* args[] = {const_cast<AttnParams*>(&p)};
-  return cudaLaunchKernelExC(&cfg, kAttnKernels[k], args);
+  e = cudaLaunchKernelExC(&cfg, kAttnKernels[k], args);
+  if (e != cudaSuccess || p.cap == 0) return e;  // no partial records: nothing to combine
+  cudaLaunchConfig_t ccfg = {};
+  ccfg.gridDim = dim3(unsigned(c->sms * kCombineBlocksPerSm));
+  ccfg.blockDim = dim3(kCombineThreads);
+  ccfg.stream = st;
+  ccfg.attrs = attr;
+  ccfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&ccfg, combine_kernel, p);
 }
 
 cudaError_t read_device_error(cudaStream_t st, uint32_t* bits, bool clear) {

@@ -51,7 +51,7 @@ extern "C" gk_status gk_decode_attn_stack_static(
   void* scratch = nullptr;
   const gk_status st = static_scratch_address(&scratch);
   if (st != GK_OK) return st;
-  // The planner rewrites the work-queue header and zeroes the split tickets
+  // The planner rewrites the work-queue header and the split-row list
   // at the start of every call, so the previous call's contents need no
   // clearing here.
   return gk_decode_attn_stack(shape, q, kv, k_scale, v_scale, cos, sin, bt_full,

@@ -86,17 +86,24 @@ def test_static_scratch_full_size_against_the_oracle():
     tl.check_out(o, of, ref, "gptoss_b64 static whole output")
 
 
-def test_static_scratch_rejects_shapes_beyond_its_size():
-    """A shape whose minimum workspace exceeds the fixed array is refused on
-    the host with GK_ERR_WORKSPACE; nothing is launched."""
+def test_static_scratch_holds_every_accepted_shape():
+    """The fixed array holds the minimum workspace of the largest shape the
+    library accepts (128 layers, batch 8192, 64 kv heads, 1024-token blocks),
+    so the no-allocation entry point refuses no valid shape for lack of room
+    (a larger array only buys more split-KV records); a shape the library
+    does not support is refused on the host before anything is launched."""
     sh = gk.Shape.make(num_layers=128, batch=8192, num_q_heads=512, num_kv_heads=64, head_dim=64,
-                       block_size=32, num_blocks=1 << 16, window=128, max_blocks_full=64,
-                       max_blocks_swa=5)
-    assert gk.gk_attn_workspace_min_bytes(sh) > (16 << 20)
+                       block_size=1024, num_blocks=1 << 16, window=128, max_blocks_full=1024,
+                       max_blocks_swa=2)
+    need = gk.gk_attn_workspace_min_bytes(sh)
+    assert 0 < need <= (16 << 20)
+    bad = gk.Shape.make(num_layers=4, batch=2, num_q_heads=16, num_kv_heads=2, head_dim=128,
+                        block_size=32, num_blocks=64, window=128, max_blocks_full=8,
+                        max_blocks_swa=5)
     good = ctypes.c_void_p(0x10000)
     arr = (ctypes.c_void_p * 64)(*([0x10000] * 64))
     kvs = gk.KvCacheC(k_bufs=ctypes.cast(arr, ctypes.c_void_p),
                       v_bufs=ctypes.cast(arr, ctypes.c_void_p), k_layout=gk.GK_K_PACKED)
-    st = gk.lib().gk_decode_attn_stack_static(ctypes.byref(sh), good, ctypes.byref(kvs),
+    st = gk.lib().gk_decode_attn_stack_static(ctypes.byref(bad), good, ctypes.byref(kvs),
                                               *([good] * 9), None, good, None, None)
-    assert st == gk.GK_ERR_WORKSPACE
+    assert st == gk.GK_ERR_UNSUPPORTED
