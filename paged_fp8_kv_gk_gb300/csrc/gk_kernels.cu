@@ -660,8 +660,11 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
 
   // the planner grid (launched just before) must be complete from here on
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // the combine grid may launch now; it waits for this grid before reading
-  asm volatile("griddepcontrol.launch_dependents;");
+  // The combine grid, launched right after this one when partial records
+  // exist (cap > 0), may launch now: it waits for this grid before reading.
+  // Without it the next launch in the stream could be a planner, which must
+  // not start (and rewrite the work queue) while this grid runs: no trigger.
+  if (p.cap > 0) asm volatile("griddepcontrol.launch_dependents;");
   const int nU = p.hdr[kHdrNUnits];
   const int nAll = nU + p.hdr[kHdrNZero];  // units with a descriptor, then zero-fill units
 
