@@ -437,10 +437,11 @@ def oracle_sample(w, c, step_host, cache, budget_s: float, seed: int = 0, k_layo
 
 
 # ------------------------------------------------------------------ end-to-end loop
-def run_e2e(gk, shape, inputs, kv, out, ws, stream, dev, K, W, units, dist):
+def run_e2e(gk, shape, inputs, kv, out, ws, stream, dev, K, W, units, dist, fused=False):
     """Time K steps fed from pinned host memory: per step one H2D copy of all
-    inputs (packed), append + attention, one D2H copy of the output.  Returns
-    (max ms over ranks, units over ranks, H2D bytes/step, D2H bytes/step)."""
+    inputs (packed), the step (gk_decode_step, or gk_kv_append +
+    gk_decode_attn_stack), one D2H copy of the output.  Returns (max ms over
+    ranks, units over ranks, H2D bytes/step, D2H bytes/step)."""
     import torch
     names = list(inputs)
     offs, off = {}, 0
@@ -485,11 +486,17 @@ def run_e2e(gk, shape, inputs, kv, out, ws, stream, dev, K, W, units, dist):
         stream.wait_event(ev_in[i])
         if k >= 2:
             stream.wait_event(ev_out[i])         # output i of step k-2 has been read back
-        gk.gk_kv_append(shape, d["k_new"], d["v_new"], d["cos"], d["sin"], d["k_scale"],
-                        d["v_scale"], d["upd_full"], d["upd_swa"], d["active"], kv, stream=sh)
-        gk.gk_decode_attn_stack(shape, d["q"], kv, d["k_scale"], d["v_scale"], d["cos"],
-                                d["sin"], d["bt_full"], d["bt_swa"], d["pos"], d["pos_w"],
-                                d["active"], outs[i], None, ws, stream=sh)
+        if fused:
+            gk.gk_decode_step(shape, d["q"], d["k_new"], d["v_new"], d["cos"], d["sin"],
+                              d["k_scale"], d["v_scale"], d["upd_full"], d["upd_swa"],
+                              d["bt_full"], d["bt_swa"], d["pos"], d["pos_w"], d["active"], kv,
+                              outs[i], None, ws, stream=sh)
+        else:
+            gk.gk_kv_append(shape, d["k_new"], d["v_new"], d["cos"], d["sin"], d["k_scale"],
+                            d["v_scale"], d["upd_full"], d["upd_swa"], d["active"], kv, stream=sh)
+            gk.gk_decode_attn_stack(shape, d["q"], kv, d["k_scale"], d["v_scale"], d["cos"],
+                                    d["sin"], d["bt_full"], d["bt_swa"], d["pos"], d["pos_w"],
+                                    d["active"], outs[i], None, ws, stream=sh)
         ev_done[i].record(stream)
         s_out.wait_event(ev_done[i])
         with torch.cuda.stream(s_out):
@@ -681,6 +688,32 @@ def measure_step(args, name, dev, dist, with_clocks=False, with_oracle=False):
         a1[k].record(stream)
     torch.cuda.synchronize(dev)
     append_ms = statistics.fmean(a0[k].elapsed_time(a1[k]) for k in range(K))
+    # the other step form, for the record (gk_kv_append + gk_decode_attn_stack
+    # beside gk_decode_step, or the reverse), timed like timed loop 1
+    def other_step():
+        if args.step == "fused":
+            append()
+            attention()
+        else:
+            fused_step()
+    for _ in range(W):
+        other_step()
+    torch.cuda.synchronize(dev)
+    if flush:
+        for k in range(K):
+            l2_flush(k)
+            a0[k].record(stream)
+            other_step()
+            a1[k].record(stream)
+        torch.cuda.synchronize(dev)
+        other_ms = sum(a0[k].elapsed_time(a1[k]) for k in range(K)) / K
+    else:
+        ev0.record(stream)
+        for k in range(K):
+            other_step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        other_ms = ev0.elapsed_time(ev1) / K
     units = gi.layer_seqs(w, c)
     max_ms, total_units = reduce_timing(elapsed_ms, units * K, dist, dev)
     value = total_units / (max_ms / 1e3)
@@ -690,7 +723,8 @@ def measure_step(args, name, dev, dist, with_clocks=False, with_oracle=False):
     # copy streams so that step k+1's upload and step k's download overlap
     # step k's kernels.
     e2e_ms, e2e_units, h2d, d2h = run_e2e(gk, shape, dict(q=q, k_new=k_new, v_new=v_new, **ctl),
-                                          kv, out, ws, stream, dev, K, W, units, dist)
+                                          kv, out, ws, stream, dev, K, W, units, dist,
+                                          fused=args.step == "fused")
     if gk.gk_read_device_error() != 0:
         raise RuntimeError(f"{name}: device error word set during the timed region")
 
@@ -705,6 +739,8 @@ def measure_step(args, name, dev, dist, with_clocks=False, with_oracle=False):
         "l2": l2_note,
         "attn_ms": round(attn_ms, 4), "attn_ms_median": round(attn_med, 4),
         "append_ms": round(append_ms, 4), "achieved_GBps": round(achieved, 1),
+        "other_step": {"form": ("gk_kv_append + gk_decode_attn_stack" if args.step == "fused"
+                                else "gk_decode_step"), "ms_per_step": round(other_ms, 4)},
         "kv_bytes_per_step": kv_bytes, "qo_bytes_per_step": gi.qo_bytes(w, c),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -720,6 +756,9 @@ def measure_step(args, name, dev, dist, with_clocks=False, with_oracle=False):
                 "ms_per_step": round(e2e_ms / K, 4), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clk,
+        # the combine kernel runs when the workspace holds partial records:
+        # the recommended workspace does once a row may exceed 512 keys
+        "combine_launched": int(not args.ws_min and c.max_blocks_full * w.block_size > 512),
     }
     if with_oracle:
         host = {k: gi.bf16_bits(v) for k, v in st.items()}
@@ -744,10 +783,13 @@ def run_gk(args):
                      "accumulation; fp32 online softmax",
         "data": "synthetic (seeded gk_inputs workload)",
         "impl": "gk",
-        "step_form": args.step + (" (CUDA graph)" if args.graph else ""),
-        "gpu_launches": (2 if args.step == "fused" else 3) * K,  # per timed step
+        "step_form": ("gk_decode_step" if args.step == "fused" else
+                      "gk_kv_append + gk_decode_attn_stack") + (" (CUDA graph)" if args.graph else ""),
+        # per timed step: (plan + append) + attention [+ split-KV combine] for
+        # gk_decode_step; append + plan + attention [+ combine] for the two calls
+        "gpu_launches": ((2 if args.step == "fused" else 3) + head["combine_launched"]) * K,
     }
-    line.update(head)
+    line.update({k: v for k, v in head.items() if k != "combine_launched"})
     if world == 1 and not args.no_per_config and args.workload == DEFAULT_WORKLOAD:
         per = {}
         for name in PER_CONFIG:
@@ -757,6 +799,7 @@ def run_gk(args):
                          "frac": r["roofline"]["frac"],
                          "frac_nominal": r["roofline"]["frac_nominal"],
                          "traffic": r["roofline"]["traffic"], "e2e": r["e2e"]["value"],
+                         "other_step_ms": r["other_step"]["ms_per_step"],
                          "alg_bytes_per_launch": r["roofline"]["alg_bytes_per_launch"],
                          "config": r["config"], "l2": r["l2"]}
             torch.cuda.empty_cache()
@@ -906,8 +949,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="measure the headline workload only (no per_config block)")
-    ap.add_argument("--step", choices=["split", "fused"], default="split",
-                    help="split: gk_kv_append + gk_decode_attn_stack; fused: gk_decode_step")
+    ap.add_argument("--step", choices=["split", "fused"], default="fused",
+                    help="fused: gk_decode_step (the append in the planner's launch; the default, "
+                         "measured faster); split: gk_kv_append + gk_decode_attn_stack")
     ap.add_argument("--k-layout", choices=["packed", "plain"], default="packed",
                     help="K through the packed view (the page's layout) or unpacked like V")
     ap.add_argument("--kv-form", choices=["per_group", "stacked"], default="per_group",
