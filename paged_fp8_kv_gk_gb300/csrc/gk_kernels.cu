@@ -499,7 +499,7 @@ __device__ __forceinline__ void plan_body(const PlanParams& p) {
   }
   if (tid == 0) {
     if (TS > p.cap) set_error(GK_DEVERR_PLAN);
-    p.hdr[kHdrQueue] = 0;
+    p.hdr[kHdrQueue] = p.n_warps;
     p.hdr[kHdrNUnits] = (NEF + NA) * planes;
     p.hdr[kHdrNZero] = (p.Bt - NA) * p.NL;
     p.hdr[kHdrSplit] = int(S);
@@ -672,11 +672,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
   // Each warp holds one claimed unit ahead of the one it streams: its
   // descriptor is loaded when it is claimed and its first block-table chunk
   // while the current unit streams.  (Claiming two ahead measured slower.)
-  int u_after = 0, u_next = 0;
-  if (lane == 0) {
-    u_next = atomicAdd(p.queue, 1);
-  }
-  u_next = __shfl_sync(kFull, u_next, 0);
+  // the first unit of warp w is unit w (the planner starts the counter at
+  // the grid's warp count): no burst of claims on one counter at the start
+  int u_after = 0, u_next = int(blockIdx.x) * kWarps + warp;
   // the claimed unit's descriptor travels into shared memory by cp.async (no
   // registers held while it is in flight); read_desc waits for it
   auto claim_desc = [&](int u) {
