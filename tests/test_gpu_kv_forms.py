@@ -91,7 +91,9 @@ def test_fused_step_unpacked_equals_two_calls():
     assert torch.equal(a.out, b.out) and torch.equal(a.out_f32, b.out_f32)
 
 
-def test_full_size_unpacked_k_sampled():
+def test_full_size_unpacked_k_whole_output():
+    """Unpacked K in the stacked form on the 36-layer batch-64 workload: every
+    appended byte bit-exact and every output element against the oracle."""
     name = "gptoss_b64"
     w = gi.get(name)
     c = gi.make_control(w)
@@ -109,18 +111,8 @@ def test_full_size_unpacked_k_sampled():
     act = c.active == 1
     assert np.array_equal(kc_d[:, act], kc_o[:, act])
     assert np.array_equal(vc_d[:, act], vc_o[:, act])
-    assert torch.isfinite(g.out_f32).all()
-    host = {k: gi.bf16_bits(v) for k, v in st.items()}
-    rng = np.random.default_rng(202)
-    actives = np.nonzero(act)[0]
-    rows = sorted(set(int(x) for x in rng.choice(actives, size=3, replace=False)))
-    G = w.num_q_heads // w.num_kv_heads
     out, of = _f64(g.out), _f64(g.out_f32)
-    for b in rows:
-        for j in (0, w.num_layers // 2 - 1):
-            res = tl.oracle_row_pair(w, c, host, pre, j, b, kvhs=(0, w.num_kv_heads - 1),
-                                     k_layout=1)
-            for (layer, kvh), ref in res.items():
-                sl = slice(kvh * G, (kvh + 1) * G)
-                tl.check_out(out[layer, b, sl], of[layer, b, sl], ref,
-                             f"{name} unpacked l{layer} b{b} h{kvh}")
+    del g
+    host = {k: gi.bf16_bits(v) for k, v in st.items()}
+    ref = tl.oracle_full_output(w, c, host, pre, k_layout=1)
+    tl.check_out(out, of, ref, f"{name} unpacked K whole output")

@@ -86,7 +86,9 @@ def test_fused_step_with_sinks_equals_two_calls():
     assert torch.equal(a.out, b.out) and torch.equal(a.out_f32, b.out_f32)
 
 
-def test_full_size_sinks_sampled():
+def test_full_size_sinks_whole_output():
+    """Attention sinks on the 36-layer batch-64 workload: every output element
+    against the oracle."""
     w = gi.get("gptoss_b64")
     c = gi.make_control(w)
     st = gi.make_step(w, "cuda")
@@ -98,15 +100,8 @@ def test_full_size_sinks_sampled():
     g.attention()
     torch.cuda.synchronize()
     assert gk.gk_read_device_error() == 0
-    host = {k: gi.bf16_bits(v) for k, v in st.items()}
-    rows = [int(x) for x in np.random.default_rng(9).choice(np.nonzero(c.active)[0], 2,
-                                                            replace=False)]
-    G = w.num_q_heads // w.num_kv_heads
     out, of = _f64(g.out), _f64(g.out_f32)
-    for b in rows:
-        for j in (0, w.num_layers // 2 - 1):
-            res = tl.oracle_row_pair(w, c, host, pre, j, b, kvhs=(0, w.num_kv_heads - 1),
-                                     sinks=sinks)
-            for (layer, kvh), ref in res.items():
-                sl = slice(kvh * G, (kvh + 1) * G)
-                tl.check_out(out[layer, b, sl], of[layer, b, sl], ref, f"sinks l{layer} b{b}")
+    del g, cache
+    host = {k: gi.bf16_bits(v) for k, v in st.items()}
+    ref = tl.oracle_full_output(w, c, host, pre, sinks=sinks)
+    tl.check_out(out, of, ref, "sinks whole output")
