@@ -108,10 +108,16 @@ def measured_peaks():
 
 
 def attn_source_hash() -> str:
+    """Hash of the attention kernel's sources with comments and blank space
+    removed (an edit of a comment is not a change of the kernel)."""
+    import re
     h = hashlib.sha256()
     for rel in ATTN_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

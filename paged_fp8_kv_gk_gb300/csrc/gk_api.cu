@@ -198,7 +198,7 @@ struct AppendInputs {
 };
 
 // Validation and launch shared by gk_decode_attn_stack and gk_decode_step
-// (app != nullptr: the single-launch step, whose planner grid also appends).
+// (app != nullptr: gk_decode_step, whose planner grid also appends).
 static gk_status decode_attention(const gk_shape* shape, const void* q, const gk_kv_cache* kv,
                                   const float* k_scale, const float* v_scale,
                                   const float* cos, const float* sin, const int32_t* bt_full,
@@ -286,7 +286,7 @@ static gk_status decode_attention(const gk_shape* shape, const void* q, const gk
   pl.force_split_log = force_split_log;
   AppendParams ap;
   if (app) {
-    // the single-launch step: the append runs in the planner's grid
+    // gk_decode_step: the append runs in the planner's grid
     memset(&ap, 0, sizeof(ap));
     ap.k_new = static_cast<const uint16_t*>(app->k_new);
     ap.v_new = static_cast<const uint16_t*>(app->v_new);

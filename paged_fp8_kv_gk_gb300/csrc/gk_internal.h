@@ -97,7 +97,7 @@ struct PlanParams {
   int force_split_log;
 };
 
-// The single-launch step's planner grid: CTA 0 plans, the others append.
+// gk_decode_step's planner grid: CTA 0 plans, the others append.
 struct PlanAppendParams {
   PlanParams plan;
   AppendParams app;
@@ -148,7 +148,7 @@ struct IngestParams {
 // Launchers (gk_kernels.cu).  They return the launch status.
 cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
 cudaError_t launch_quantize(const float* x, float scale, uint8_t* codes, int64_t n, cudaStream_t st);
-// app: the single-launch step's append, done in the planner's grid (or null).
+// app: gk_decode_step's append, done in the planner's grid (or null).
 cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaStream_t st,
                              const AppendParams* app = nullptr);
 // Resident warps of the persistent attention grid on the current device.

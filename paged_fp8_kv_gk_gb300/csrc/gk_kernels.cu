@@ -3,9 +3,9 @@
 //   kv_append_kernel   RoPE(k) in IEEE fp32, / scale, E4M3 (RNE, satfinite),
 //                      scatter into the packed K and plain V layouts.
 //   plan_kernel        one CTA: split-KV chunk length, work-unit order
-//                      (largest first), per-row split bookkeeping; in the
-//                      single-launch step, further CTAs of the same grid do
-//                      the KV append beside it.
+//                      (largest first), per-row split bookkeeping; for
+//                      gk_decode_step, further CTAs of the same grid do the
+//                      KV append beside it (plan_append_kernel).
 //   attn_kernel        persistent: each warp takes (layer, row, kv head, split)
 //                      units from an atomic counter, streams 32-token stages of
 //                      K and V through a private ring of 1-D bulk copies, and
@@ -51,13 +51,11 @@ __device__ __forceinline__ float div_scale(float x, float s, float r) {
 // One warp per (layer i, row b); kv heads in groups of 8.  Lane l rotates
 // the pair (l, l + 32) of k and converts channels 2l, 2l + 1 of v.  All of a
 // group's loads are issued before any of them is used (one memory round trip
-// per group rather than a chain of dependent ones).  P is AppendParams (the
-// append kernel) or AttnParams (the single-launch step, whose attention warps
-// append while the planner runs); ib = i * Bt + b.
+// per group rather than a chain of dependent ones).  Used by the append kernel
+// and by the append CTAs of gk_decode_step's planner launch; ib = i * Bt + b.
 constexpr int kAppendHeads = 8;
 
-template <class P>
-__device__ __forceinline__ void append_row(const P& p, int64_t ib, int lane) {
+__device__ __forceinline__ void append_row(const AppendParams& p, int64_t ib, int lane) {
   const int b = int(ib % p.Bt);
   const int i = int(ib / p.Bt);
   const uint16_t* kr = p.k_new + ib * p.Hkv * kHeadDim;
@@ -91,12 +89,12 @@ __device__ __forceinline__ void append_row(const P& p, int64_t ib, int lane) {
     // packed K: tokens 2p and 2p+1 interleaved per channel (channel e at byte
     // 2e of the pair row); plain K: laid out like V.  Either way a head's block
     // is B * D bytes.
-    uint8_t* kbase = const_cast<uint8_t*>(p.kb[i >> 1]);
+    uint8_t* kbase = p.kb[i >> 1];
     uint8_t* kdst = p.k_packed
                         ? kbase + ((pb * p.Hkv + h0) * (p.B >> 1) + (t >> 1)) * (2 * kHeadDim) + (t & 1)
                         : kbase + ((pb * p.Hkv + h0) * p.B + t) * kHeadDim;
     const int estep = p.k_packed ? 2 : 1;
-    uint8_t* vdst = const_cast<uint8_t*>(p.vb[i >> 1]) + ((pb * p.Hkv + h0) * p.B + t) * kHeadDim;
+    uint8_t* vdst = p.vb[i >> 1] + ((pb * p.Hkv + h0) * p.B + t) * kHeadDim;
     const int64_t kstride = int64_t(p.B) * kHeadDim, vstride = int64_t(p.B) * kHeadDim;
 #pragma unroll
     for (int k = 0; k < kAppendHeads; ++k) {
@@ -520,7 +518,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   plan_body(p);
 }
 
-// Single-launch step: CTA 0 plans; the CTAs after it append the new token,
+// gk_decode_step: CTA 0 plans; the CTAs after it append the new token,
 // warp w taking (layer, row) pairs w, w + warps, ...  The attention grid waits
 // for this whole grid, so it reads the plan and the appended cache; the kernel
 // before this grid must be complete before the cache is written.
@@ -1548,7 +1546,7 @@ cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaSt
   pcfg.attrs = attr;
   pcfg.numAttrs = 1;
   if (app) {
-    // the single-launch step appends in CTAs beside the planner's: one warp
+    // gk_decode_step appends in CTAs beside the planner's: one warp
     // per (layer, row) pair
     PlanAppendParams pa;
     pa.plan = pp;

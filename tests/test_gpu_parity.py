@@ -80,7 +80,7 @@ def test_one_key_rows_return_value_exactly(name):
 @pytest.mark.parametrize("name", ["long_small", "gptoss_small", "ragged_small"])
 def test_split_and_unsplit_agree(name):
     """The recommended workspace lets the planner split long rows (flash-
-    decoding partials merged by the last split); the minimum workspace forces
+    decoding partials merged by the combine kernel); the minimum workspace forces
     one unit per row.  Both must meet the tolerance, and the split run must
     actually have split."""
     w, c, st, cache = _make_cpu(name)

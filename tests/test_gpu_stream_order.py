@@ -5,7 +5,7 @@ The planner, the attention grid and the split-KV combine are chained by
 programmatic dependent launches; a later call's planner rewrites the work
 queue in the shared workspace, so it must not start while an earlier call's
 attention grid still takes units from it.  Two alternating inputs (different
-q, and for the single-launch step different new tokens appended at the same
+q, and for gk_decode_step different new tokens appended at the same
 slots) make any unit done with the other call's arguments, or skipped, show
 up as a mismatch or a NaN left in a NaN-filled output.  Run with and without
 partial records (a workload whose rows can split, and one whose rows cannot),
