@@ -191,7 +191,11 @@ size_t gk_attn_workspace_min_bytes(const gk_shape *shape);
  * first on the same stream when the new token must be attended to.
  * workspace: device memory, 256-byte aligned, ws_bytes >= gk_attn_workspace_min_bytes;
  * it is overwritten by every call (do not share one workspace between calls
- * that may overlap on the device).
+ * that may overlap on the device).  Calls issued one after another on one
+ * stream are ordered: a call runs a planner, the attention grid and, when
+ * rows are split across warps, a combine grid, chained by programmatic
+ * dependent launches, and the next call's planner starts only once this
+ * call no longer reads the workspace.
  * Returns GK_ERR_WORKSPACE for a missing/small/misaligned workspace,
  * GK_ERR_INVALID_ARG for null or non-16-byte-aligned tensors (sinks: 4-byte)
  * or a kv that does not hold exactly one form.

@@ -281,7 +281,7 @@ __device__ __forceinline__ void plan_body(const PlanParams& p) {
     while (k < kSplitCands - 1 && ((long long)kMinSplit << k) < share) ++k;
     while (k > 0 && (s_units[k] + NAct) * planes < kUnitsPerWarp * warps) --k;
     // no short chunks that would give a row more than kShortMerge partials:
-    // their serial merge outweighs the balance they buy
+    // the per-unit cost of the extra partials outweighs the balance they buy
     while (k < kSplitCands - 1 && ((long long)kMinSplit << k) <= kShortSplit &&
            (Lmax - 1) / ((long long)kMinSplit << k) + 1 > kShortMerge)
       ++k;
