@@ -1317,15 +1317,20 @@ __global__ void __launch_bounds__(kWarps * 32, kMma ? 4 : 3)
 // One warp per (split row, plane = (layer pair j, kv head)) merges the ns
 // partial records of full layer 2j + 1, row b, kv head into the output.  Lane
 // (g, qd) produces heads 2qd, 2qd + 1, channels 8g .. 8g + 7.  The partials
-// are read kCombineAhead at a time (their loads in flight together) and
+// are read kAhead at a time (their loads in flight together) and
 // folded in split order -- the same order whatever order the splits finished
 // in -- with a running maximum; then the output scale (attention sink
 // included) and the bf16 (+ fp32) stores.
+// Two forms.  The kernel is a chain of dependent rounds of partial loads:
+// when every item fits in one wave of warps, eight partials per round at two
+// CTAs per SM (211 registers) finish sooner; with more items than that, four
+// per round at four CTAs per SM keep more items in flight.
 constexpr int kCombineThreads = 128;
-constexpr int kCombineBlocksPerSm = 4;
-constexpr int kCombineAhead = 4;
+constexpr int kCombineDeepAhead = 8, kCombineDeepBlocks = 2;
+constexpr int kCombineAhead = 4, kCombineBlocks = 4;
 
-__global__ void __launch_bounds__(kCombineThreads, kCombineBlocksPerSm)
+template <int kAhead, int kBlocksPerSm>
+__global__ void __launch_bounds__(kCombineThreads, kBlocksPerSm)
     combine_kernel(const __grid_constant__ AttnParams p) {
   // the attention grid (launched just before) must be complete: its partials
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1348,11 +1353,11 @@ __global__ void __launch_bounds__(kCombineThreads, kCombineBlocksPerSm)
     float a0[8], a1[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) a0[c] = a1[c] = 0.f;
-    for (int s0 = 0; s0 < ns; s0 += kCombineAhead) {
-      float2 ms[kCombineAhead], ls[kCombineAhead];
-      float4 o00[kCombineAhead], o01[kCombineAhead], o10[kCombineAhead], o11[kCombineAhead];
+    for (int s0 = 0; s0 < ns; s0 += kAhead) {
+      float2 ms[kAhead], ls[kAhead];
+      float4 o00[kAhead], o01[kAhead], o10[kAhead], o11[kAhead];
 #pragma unroll
-      for (int k = 0; k < kCombineAhead; ++k) {
+      for (int k = 0; k < kAhead; ++k) {
         if (s0 + k < ns) {
           const float* rs = base + int64_t(s0 + k) * kPartialFloats;
           ms[k] = ldg_cg_f2(rs + 2 * qd);
@@ -1365,7 +1370,7 @@ __global__ void __launch_bounds__(kCombineThreads, kCombineBlocksPerSm)
         }
       }
 #pragma unroll
-      for (int k = 0; k < kCombineAhead; ++k) {
+      for (int k = 0; k < kAhead; ++k) {
         if (s0 + k < ns) {
           const float n0 = fmaxf(M0, ms[k].x), n1 = fmaxf(M1, ms[k].y);
           const float c0 = ex2(M0 - n0), w0 = ex2(ms[k].x - n0);
@@ -1569,13 +1574,18 @@ cudaError_t launch_attention(const PlanParams& plan, const AttnParams& p, cudaSt
   void* args[] = {const_cast<AttnParams*>(&p)};
   e = cudaLaunchKernelExC(&cfg, kAttnKernels[k], args);
   if (e != cudaSuccess || p.cap == 0) return e;  // no partial records: nothing to combine
+  // the deep form when even batch x planes items (every row split) fit in
+  // one wave of its warps
+  const bool deep = int64_t(p.Bt) * int64_t(p.fd_planes.d) <=
+                    int64_t(c->sms) * kCombineDeepBlocks * (kCombineThreads / 32);
   cudaLaunchConfig_t ccfg = {};
-  ccfg.gridDim = dim3(unsigned(c->sms * kCombineBlocksPerSm));
+  ccfg.gridDim = dim3(unsigned(c->sms * (deep ? kCombineDeepBlocks : kCombineBlocks)));
   ccfg.blockDim = dim3(kCombineThreads);
   ccfg.stream = st;
   ccfg.attrs = attr;
   ccfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&ccfg, combine_kernel, p);
+  return deep ? cudaLaunchKernelEx(&ccfg, combine_kernel<kCombineDeepAhead, kCombineDeepBlocks>, p)
+              : cudaLaunchKernelEx(&ccfg, combine_kernel<kCombineAhead, kCombineBlocks>, p);
 }
 
 cudaError_t read_device_error(cudaStream_t st, uint32_t* bits, bool clear) {
