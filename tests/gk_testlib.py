@@ -32,6 +32,11 @@ def ulp_bf16(x: np.ndarray) -> np.ndarray:
     return np.where(a > 0, 2.0 ** (e - 7), 2.0 ** -133)
 
 
+# (what, statistics) of every check_out call of the session, listed by the
+# terminal summary (tests/conftest.py) so that a quiet run still shows them
+REPORT = []
+
+
 def check_out(out_bf16: np.ndarray, out_f32, ref: np.ndarray, what: str = ""):
     """out_bf16: float64 view of the kernel's bf16 output; out_f32 may be None.
     Returns the error statistics, with `bf16_widened`: how many bf16 elements
@@ -53,6 +58,7 @@ def check_out(out_bf16: np.ndarray, out_f32, ref: np.ndarray, what: str = ""):
         stats.update(f32_max=float(e.max()), f32_mean=float(e.mean()))
     print("check_out", what, {k: (round(v, 6) if isinstance(v, float) else v)
                               for k, v in stats.items()})
+    REPORT.append((what, stats))
     return stats
 
 

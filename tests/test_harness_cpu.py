@@ -109,3 +109,23 @@ def test_bench_records_traffic_from_an_ncu_launch_list(tmp_path, monkeypatch):
     # a capture taken on another kernel source is not used
     monkeypatch.setattr(bench, "attn_source_hash", lambda: "0" * 16)
     assert bench.recorded_traffic(full, cf) is None
+
+
+def test_check_out_counts_the_one_step_allowance():
+    """The bf16 bar: 1.5e-2 absolute, widened to one bf16 step where that step
+    is larger (|x| >= 4, step 2^-5); every widened element is counted and
+    listed in the session's report."""
+    import oracle
+    ref = oracle.round_bf16(np.linspace(-8.0, 8.0, 1001))
+    out = ref.copy()
+    big = np.flatnonzero(np.abs(ref) >= 4.0)[:3]
+    small = np.flatnonzero(np.abs(ref) < 1.0)[0]
+    out[big] += np.array([0.02, 0.025, 0.03])   # beyond 1.5e-2, within one step
+    out[small] += 0.01                          # within 1.5e-2
+    n0 = len(tl.REPORT)
+    st = tl.check_out(out, None, ref, "allowance probe")
+    assert st["bf16_widened"] == 3 and st["elements"] == ref.size
+    assert tl.REPORT[n0:] == [("allowance probe", st)]
+    out[small] += 0.01                          # 0.02 where the step is 2^-8: too far
+    with pytest.raises(AssertionError):
+        tl.check_out(out, None, ref, "too far")
